@@ -1,0 +1,156 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact tiled attention library.
+ *
+ * The library computes exact scaled-dot-product attention in the
+ * FlashAttention style: blockwise Q K^T, an FP32 online softmax (running
+ * row max and row sum, rescaling of the partial output) and blockwise P V,
+ * forward and backward.  The operation is the "Baseline Attention" of
+ * "Is Flash Attention Stable?" (abstract): O = softmax(scale * Q K^T) V, with
+ * an optional causal mask; its tiled evaluation follows the block division
+ * of "Why Low-Precision Transformer Training Fails", Algorithm 1 (Q split
+ * into row blocks, K and V into column blocks).  The backward pass uses
+ * delta = rowsum(dO o O) as defined in that paper (Figures 3 and 5).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d], contiguous,
+ *    d fastest, in DEVICE memory (device or managed allocations), 16-byte
+ *    aligned.  LSE is FP32 [B, H, N] (natural log): LSE_i = ln sum_j
+ *    exp(scale * q_i . k_j) over the visible keys.
+ *  - causal != 0 hides key j from query i when j > i (square, top-left).
+ *  - dt selects the element type of Q, K, V, O, dO, dQ, dK, dV:
+ *      ATTN_DTYPE_BF16 -- tensor-core path (TMA + tcgen05/TMEM), FP32
+ *                         softmax and accumulation, BF16 results;
+ *      ATTN_DTYPE_FP32 -- reference mode: the same tiled online softmax in
+ *                         FP32 CUDA-core arithmetic (no tensor cores).
+ *  - Supported: d in {64, 128}; N >= 1; B*H*N*d < 2^31; scale finite > 0.
+ *  - Ownership: the caller allocates every buffer and owns the stream; the
+ *    library allocates no device memory and keeps no per-call state.
+ *  - Asynchrony: kernels are enqueued on `stream` and the call returns
+ *    without synchronizing.  Argument errors are reported synchronously,
+ *    before anything is enqueued; launch failures map to ATTN_ERR_CUDA.
+ *  - Every wait inside a kernel is bounded (about 2 s).  A wait that gives
+ *    up records ATTN_ERR_TIMEOUT on the device and the kernel returns;
+ *    attn_check_status() reports it.
+ *  - The device is the one current on the calling thread; all pointers
+ *    must belong to it.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* bad pointer, shape, scale or workspace size */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request outside the supported set     */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed           */
+  ATTN_ERR_TIMEOUT = 4      /* a bounded in-kernel wait gave up            */
+} attn_status;
+
+typedef enum { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_FP32 = 1 } attn_dtype;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+ATTN_API int attn_version(void);
+
+/* Static description of a status code. */
+ATTN_API const char* attn_status_string(attn_status s);
+
+/* Human-readable detail of the last error returned on the calling thread
+ * (empty string when none).  The pointer stays valid until the next call on
+ * the same thread. */
+ATTN_API const char* attn_last_error(void);
+
+/*
+ * Forward pass ("Is Flash Attention Stable?", abstract: Baseline Attention;
+ * tiled as in "Why Low-Precision Transformer Training Fails", Algorithm 1).
+ *   q, k, v : [B,H,N,d] inputs (dt).
+ *   o       : [B,H,N,d] output (dt), O = softmax(scale Q K^T [+mask]) V.
+ *   lse     : [B,H,N] FP32 output, natural-log log-sum-exp of each row of
+ *             scale Q K^T over the visible keys.
+ * Returns ATTN_OK once the kernel is enqueued.
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int N, int d, float scale, int causal, attn_dtype dt,
+                              cudaStream_t stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for this problem (0 on invalid
+ * arguments).  Layout (internal): LSE*log2(e) and delta, FP32 [B*H][Npad]
+ * each, and the FP32 dQ accumulator [B*H][Npad][d], Npad = N rounded up to
+ * 128.  The workspace needs no initialisation; attn_bwd overwrites it.
+ */
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d, attn_dtype dt);
+
+/*
+ * Backward pass from the saved LSE: dQ, dK, dV of L = sum(dO o O).
+ * The gradient of the attention definition, with delta = rowsum(dO o O)
+ * ("Why Low-Precision Transformer Training Fails", Figures 3 and 5),
+ * dS = P o (dO V^T - delta), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
+ *   q, k, v, o, dout : [B,H,N,d] inputs (dt); o is the forward output.
+ *   lse              : [B,H,N] FP32, the forward's LSE.
+ *   dq, dk, dv       : [B,H,N,d] outputs (dt).
+ *   workspace        : device buffer of at least
+ *                      attn_bwd_workspace_bytes(...) bytes, 256-byte aligned,
+ *                      not shared with a concurrently running call.
+ * Enqueues three kernels on `stream`: preprocess (delta, LSE*log2(e), zero
+ * the dQ accumulator), the main kernel (dK, dV, dQ accumulation), and the
+ * dQ conversion (scale and round).  The three phases are also exported
+ * below so that each can be timed on its own.
+ */
+ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, int causal, attn_dtype dt,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Phase 1 of attn_bwd (BF16 only): delta_i = rowsum(dO o O)_i in FP32 from
+ * the stored O, LSE*log2(e), and a zeroed dQ accumulator, into `workspace`. */
+ATTN_API attn_status attn_bwd_preprocess(const void* o, const float* lse, const void* dout, int B,
+                                         int H, int N, int d, attn_dtype dt, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream);
+
+/* Phase 2 of attn_bwd (BF16 only): dK and dV (written to dk, dv) and the FP32
+ * dQ accumulation into `workspace`; needs phase 1 to have run on it. */
+ATTN_API attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout,
+                                   void* dk, void* dv, int B, int H, int N, int d, float scale,
+                                   int causal, attn_dtype dt, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
+/* Phase 3 of attn_bwd (BF16 only): dQ = bf16(scale * accumulator). */
+ATTN_API attn_status attn_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale,
+                                         attn_dtype dt, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device-side status words
+ * of the library on the current device.  Returns ATTN_ERR_TIMEOUT if any
+ * kernel gave up on a bounded wait since the last check, ATTN_ERR_CUDA if
+ * the stream reports an error, else ATTN_OK.
+ */
+ATTN_API attn_status attn_check_status(cudaStream_t stream);
+
+/*
+ * Self-test of the bounded-wait path: enqueues a one-block kernel that waits
+ * on a shared-memory barrier nothing ever arrives at, for at most limit_ns
+ * nanoseconds (1 <= limit_ns <= 10^9), then records ATTN_ERR_TIMEOUT and
+ * returns.  attn_check_status() afterwards must report ATTN_ERR_TIMEOUT.
+ */
+ATTN_API attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

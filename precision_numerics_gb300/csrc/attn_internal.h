@@ -1,0 +1,76 @@
+// Internal launch interface shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+namespace attn {
+
+// Problem description after validation.  Tensors are [B, H, N, d],
+// contiguous, d fastest; LSE is [B, H, N].
+struct Problem {
+  int B, H, N, d;
+  float scale;
+  int causal;
+};
+
+// Tile geometry of the BF16 tensor-core path.
+constexpr int kBlockM = 128;  // query rows per tile (one TMEM lane per row)
+constexpr int kBlockN = 128;  // key rows per tile
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline int n_pad(int N) { return ceil_div(N, kBlockN) * kBlockN; }
+
+// Backward workspace layout (all offsets 256-byte aligned):
+//   lse2  FP32 [B*H][Npad]    LSE * log2(e); +inf for padded rows
+//   delta FP32 [B*H][Npad]    rowsum(dO o O); 0 for padded rows
+//   dqacc FP32 [B*H][Npad][d] unscaled dQ accumulator
+struct BwdWorkspace {
+  float* lse2;
+  float* delta;
+  float* dqacc;
+};
+size_t bwd_workspace_bytes(const Problem& p);
+BwdWorkspace bwd_workspace_carve(void* base, const Problem& p);
+
+// Kernel launchers.  Return cudaSuccess or the launch error.
+cudaError_t launch_fwd_bf16(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                            float* lse, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess_bf16(const Problem& p, const void* o, const void* dout,
+                                       const float* lse, const BwdWorkspace& ws,
+                                       cudaStream_t stream);
+cudaError_t launch_bwd_main_bf16(const Problem& p, const void* q, const void* k, const void* v,
+                                 const void* dout, void* dk, void* dv, const BwdWorkspace& ws,
+                                 cudaStream_t stream);
+cudaError_t launch_bwd_dq_convert_bf16(const Problem& p, const BwdWorkspace& ws, void* dq,
+                                       cudaStream_t stream);
+
+cudaError_t launch_fwd_fp32(const Problem& p, const float* q, const float* k, const float* v,
+                            float* o, float* lse, cudaStream_t stream);
+cudaError_t launch_bwd_fp32(const Problem& p, const float* q, const float* k, const float* v,
+                            const float* o, const float* lse, const float* dout, float* dq,
+                            float* dk, float* dv, const BwdWorkspace& ws, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
+// Device status words (one per kernel translation unit): read and clear.
+cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream);
+cudaError_t read_and_clear_status_bwd(unsigned int* out, cudaStream_t stream);
+cudaError_t read_and_clear_status_misc(unsigned int* out, cudaStream_t stream);
+
+// Driver entry point for cuTensorMapEncodeTiled (resolved once, no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// 3-D BF16 tensor map over a [B*H, N, d] tensor with a (64 x 128 x 1) box and
+// 128-byte swizzle.  Returns false when the driver rejects it.
+bool make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d);
+
+}  // namespace attn

@@ -1,0 +1,600 @@
+// BF16 attention backward for sm_103a from the saved LSE.
+//
+// What is computed (the gradient of softmax attention for L = sum(dO o O)):
+//   delta_i = rowsum(dO o O)_i      ("Why Low-Precision Transformer Training
+//                                     Fails", Figures 3 and 5), from the
+//                                     stored BF16 O, in FP32
+//   P_ij    = exp(scale q_i.k_j - LSE_i)          (recomputed, causal mask)
+//   dV      = P^T dO
+//   dP      = dO V^T
+//   dS      = P o (dP - delta)
+//   dK      = scale dS^T Q,   dQ = scale dS K
+//
+// Three kernels, in stream order:
+//   1. preprocess   delta, LSE * log2(e) (+inf on padded rows, so the
+//                   recomputed P of a padded query row is exactly 0), and a
+//                   zeroed FP32 dQ accumulator.  Memory-bound.
+//   2. main         one CTA per (b, h, 128-key tile j), K_j and V_j resident in
+//                   shared memory; the CTA walks the query tiles i (causal:
+//                   i >= j) with Q_i, dO_i, LSE_i, delta_i streamed by TMA.
+//                   Per tile, five tcgen05 MMAs (128 x 128 x 128 each):
+//                     S^T  = K_j Q_i^T            (SS)  -> TMEM
+//                     dP^T = V_j dO_i^T           (SS)  -> TMEM
+//                     dV  += P^T dO_i             (TS, P^T in TMEM)
+//                     dK  += dS^T Q_i             (TS, dS^T in TMEM)
+//                     dQ_i = dS K_j               (SS, dS from shared memory)
+//                   and dQ_i is added into the FP32 accumulator with vector
+//                   reductions.  Warp roles: 0 TMA producer, 1 MMA issuer,
+//                   2 TMEM owner, 4-7 P / dS compute (one key row per thread),
+//                   8-11 dQ drain; the epilogue writes dV (warps 4-7) and
+//                   scale * dK (warps 8-11) with TMA stores.
+//   3. dq_convert   dQ = bf16(scale * accumulator).  Memory-bound.
+//
+// TMEM (512 columns): dV [0,d), dK [d,2d), S^T [2d,2d+128), dP^T
+// [2d+128,2d+256).  For d = 128 the dQ tile reuses the S^T columns (the MMA
+// that reads P^T from there is issued first, and tcgen05 MMAs of one thread
+// execute in order); for d = 64 it has its own columns [384,448).
+#include <math.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+static __device__ unsigned int g_status_bwd;
+
+namespace {
+
+__device__ __forceinline__ void set_fail(unsigned int code) { atomicOr(&g_status_bwd, code); }
+
+// ---------------------------------------------------------------------------
+// 1. preprocess
+// ---------------------------------------------------------------------------
+// Each group of d/8 threads handles one padded row; each thread owns 8
+// consecutive columns (16 bytes of O and of dO, 32 bytes of the accumulator).
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                          const float* __restrict__ lse, float* __restrict__ lse2,
+                          float* __restrict__ delta, float4* __restrict__ dqacc, int N, int Npad) {
+  constexpr int kGroup = D / 8;
+  constexpr int kRows = 256 / kGroup;
+  const int bh = blockIdx.y;
+  const int row = blockIdx.x * kRows + threadIdx.x / kGroup;
+  const int part = threadIdx.x % kGroup;
+  const bool active = row < Npad;
+  float s = 0.f;
+  if (active && row < N) {
+    const size_t idx = ((size_t)bh * N + row) * kGroup + part;
+    const uint4 a = o[idx], b = dout[idx];
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s = fmaf(__uint_as_float(av[i] << 16), __uint_as_float(bv[i] << 16), s);
+      s = fmaf(__uint_as_float(av[i] & 0xFFFF0000u), __uint_as_float(bv[i] & 0xFFFF0000u), s);
+    }
+  }
+#pragma unroll
+  for (int off = kGroup / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (!active) return;
+  const size_t prow = (size_t)bh * Npad + row;
+  if (part == 0) {
+    delta[prow] = s;
+    lse2[prow] = row < N ? lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
+  }
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  dqacc[prow * (D / 4) + 2 * part] = z;
+  dqacc[prow * (D / 4) + 2 * part + 1] = z;
+}
+
+// ---------------------------------------------------------------------------
+// 3. dq_convert
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_dq_convert_kernel(const float4* __restrict__ dqacc, uint4* __restrict__ dq, int N,
+                          int Npad, float scale, int total_units) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;  // one unit = 8 columns of one row
+  if (u >= total_units) return;
+  constexpr int kUnitsPerRow = D / 8;
+  const int col8 = u % kUnitsPerRow;
+  const int row = (u / kUnitsPerRow) % N;
+  const int bh = u / (kUnitsPerRow * N);
+  const size_t src = ((size_t)bh * Npad + row) * (D / 4) + 2 * col8;
+  const float4 a = dqacc[src], b = dqacc[src + 1];
+  uint4 out;
+  out.x = pack_bf16x2(a.x * scale, a.y * scale);
+  out.y = pack_bf16x2(a.z * scale, a.w * scale);
+  out.z = pack_bf16x2(b.x * scale, b.y * scale);
+  out.w = pack_bf16x2(b.z * scale, b.w * scale);
+  dq[u] = out;
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel
+// ---------------------------------------------------------------------------
+constexpr int kThreads = 384;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = 128 * 128;   // 128 rows x 128 bytes
+  static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x d BF16
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;        // 2 stages
+  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;   // 2 stages
+  static constexpr int kOffDS = kOffDO + 2 * kTileBytes;  // 128 key rows x 128 query cols BF16
+  static constexpr int kDSBytes = 128 * 128 * 2;
+  static constexpr int kOffLse = kOffDS + kDSBytes;    // 2 stages x 128 FP32
+  static constexpr int kOffDelta = kOffLse + 2 * 512;  // 2 stages x 128 FP32
+  static constexpr int kOffBar = kOffDelta + 2 * 512;
+  // kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_ready, ds_ready,
+  // dq_full, dq_free, dkv_done, mma_final
+  static constexpr int kNumBars = 13;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
+  static constexpr uint32_t kColDV = 0;
+  static constexpr uint32_t kColDK = D;
+  static constexpr uint32_t kColS = 2 * D;
+  static constexpr uint32_t kColDP = 2 * D + 128;
+  static constexpr uint32_t kColDQ = (D == 128) ? kColS : 384u;
+  static constexpr bool kDqAliasesS = (D == 128);
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
+                    const float* __restrict__ lse2, const float* __restrict__ delta,
+                    float* __restrict__ dqacc, int BH, int N, int Npad, float scale,
+                    float scale_log2) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_qt = Npad / kBlockM;
+
+  // Key tiles with the most query tiles (causal: small j) first.
+  const int j = blockIdx.x / BH;
+  const int bh = blockIdx.x % BH;
+  const int i_first = CAUSAL ? j : 0;
+  const int nq = n_qt - i_first;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* bar_kv = bars + 0;
+  uint64_t* bar_qfull = bars + 1;   // [2]
+  uint64_t* bar_qempty = bars + 3;  // [2]
+  uint64_t* bar_sfull = bars + 5;
+  uint64_t* bar_dpfull = bars + 6;
+  uint64_t* bar_pready = bars + 7;
+  uint64_t* bar_dsready = bars + 8;
+  uint64_t* bar_dqfull = bars + 9;
+  uint64_t* bar_dqfree = bars + 10;
+  uint64_t* bar_dkvdone = bars + 11;
+  uint64_t* bar_final = bars + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+
+  if (threadIdx.x == 0) {
+    s_abort = (smem_u32(smem) & 1023u) != 0;
+    if (s_abort) set_fail(ATTN_ERR_INVALID_ARG);
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_qfull[s], 1);
+      mbar_init(&bar_qempty[s], 1 + 4);  // MMA commit + one arrive per compute warp
+    }
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_dpfull, 1);
+    mbar_init(bar_pready, 128);
+    mbar_init(bar_dsready, 128);
+    mbar_init(bar_dqfull, 1);
+    mbar_init(bar_dqfree, 128);
+    mbar_init(bar_dkvdone, 1);
+    mbar_init(bar_final, 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool abort_all = s_abort != 0;
+
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sDO = smem + C::kOffDO;
+  uint8_t* sDS = smem + C::kOffDS;
+  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* sDelta = reinterpret_cast<float*>(smem + C::kOffDelta);
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (warp == 0 && lane == 0 && !abort_all) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(sK + c * C::kChunkBytes, &tmK, bar_kv, c * 64, j * kBlockN, bh);
+        tma_load_3d(sV + c * C::kChunkBytes, &tmV, bar_kv, c * 64, j * kBlockN, bh);
+      }
+      bool ok = true;
+      int issued = 0;
+      for (int it = 0; it < nq; ++it) {
+        const int st = it & 1, use = it >> 1;
+        const int i = i_first + it;
+        if (use > 0 && !mbar_wait(&bar_qempty[st], (use - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bar_qfull[st], 2 * C::kTileBytes + 2 * 512);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(sQ + st * C::kTileBytes + c * C::kChunkBytes, &tmQ, &bar_qfull[st], c * 64,
+                      i * kBlockM, bh);
+          tma_load_3d(sDO + st * C::kTileBytes + c * C::kChunkBytes, &tmDO, &bar_qfull[st], c * 64,
+                      i * kBlockM, bh);
+        }
+        const size_t prow = (size_t)bh * Npad + (size_t)i * kBlockM;
+        bulk_load(sLse + st * 128, lse2 + prow, 512, &bar_qfull[st]);
+        bulk_load(sDelta + st * 128, delta + prow, 512, &bar_qfull[st]);
+        issued = it + 1;
+      }
+      if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      mbar_wait(bar_kv, 0);
+      for (int it = max(0, issued - 2); it < issued; ++it)
+        mbar_wait(&bar_qfull[it & 1], (it >> 1) & 1);
+    } else if (warp == 1 && lane == 0 && !abort_all) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);  // K-major A and B
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // TMEM A, MN-major B
+      constexpr uint32_t idesc_dq = idesc_bf16(128, D, true, true);     // MN-major A and B
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ),
+                     aDO = smem_u32(sDO), aDS = smem_u32(sDS);
+      bool ok = mbar_wait(bar_kv, 0);
+      for (int it = 0; it < nq && ok; ++it) {
+        const int st = it & 1, use = it >> 1;
+        if (!mbar_wait(&bar_qfull[st], use & 1)) { ok = false; break; }
+        if (C::kDqAliasesS && it > 0 && !mbar_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qoff = aQ + st * C::kTileBytes, dooff = aDO + st * C::kTileBytes;
+        // S^T = K_j Q_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kColS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(qoff + off, 16, 1024),
+                 idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_sfull);
+        // dP^T = V_j dO_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDP, sdesc_sw128(aV + off, 16, 1024),
+                 sdesc_sw128(dooff + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_dpfull);
+        // dV += P^T dO_i
+        if (!mbar_wait(bar_pready, it & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk)
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                 sdesc_sw128(dooff + kk * 2048, C::kChunkBytes, 1024), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i
+        if (!mbar_wait(bar_dsready, it & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk)
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                 sdesc_sw128(qoff + kk * 2048, C::kChunkBytes, 1024), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_qempty[st]);
+        // dQ_i = dS K_j
+        if (!C::kDqAliasesS && it > 0 && !mbar_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ss(tmem + C::kColDQ, sdesc_sw128(aDS + kk * 2048, C::kChunkBytes, 1024),
+                 sdesc_sw128(aK + kk * 2048, C::kChunkBytes, 1024), idesc_dq, kk > 0 ? 1u : 0u);
+        mma_commit(bar_dqfull);
+      }
+      if (ok) mma_commit(bar_dkvdone);
+      else set_fail(ATTN_ERR_TIMEOUT);
+      mma_commit(bar_final);
+      mbar_wait(bar_final, 0);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    // -------------------------------------------------- P and dS (key rows)
+    const int r = (warp & 3) * 32 + lane;  // key row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::kColS;
+    const uint32_t tDP = tmem + lane_off + C::kColDP;
+    const bool key_valid = j * kBlockN + r < N;
+    const uint32_t aDS = smem_u32(sDS);
+    bool ok = !abort_all;
+    for (int it = 0; it < nq && ok; ++it) {
+      const int st = it & 1, use = it >> 1;
+      const int i = i_first + it;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_qfull[st], use & 1));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_sfull, it & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t p[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, p[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence(p[c]);
+      const float* L2 = sLse + st * 128;
+      // Keys after the query (diagonal tile only) and padded keys get P = 0;
+      // padded queries have LSE*log2(e) = +inf, so their P is 0 already.
+      const int vis_from = (CAUSAL && i == j) ? r : 0;  // query columns c >= vis_from visible
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cc = c + e;
+          float pv = ex2(fmaf(__uint_as_float(p[cc >> 5][cc & 31]), scale_log2, -lv[e]));
+          if (!key_valid || cc < vis_from) pv = 0.f;
+          p[cc >> 5][cc & 31] = __float_as_uint(pv);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(p[c][2 * e]), __uint_as_float(p[c][2 * e + 1]));
+        tmem_st16(tS + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_pready);
+
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dpfull, it & 1));
+      if (!ok) break;
+      // The dS buffer in shared memory is free once the previous dQ MMA is done.
+      if (it > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_dqfull, (it - 1) & 1));
+        if (!ok) break;
+      }
+      tc_fence_after();
+      const float* Dl = sDelta + st * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32];
+        tmem_ld32(tDP + c * 32, dp);
+        tmem_wait_ld();
+        reg_fence(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = c * 32 + 2 * e;
+          const float2 d2 = *reinterpret_cast<const float2*>(Dl + c0);
+          const float ds0 = __uint_as_float(p[c][2 * e]) * (__uint_as_float(dp[2 * e]) - d2.x);
+          const float ds1 = __uint_as_float(p[c][2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - d2.y);
+          pk[e] = pack_bf16x2(ds0, ds1);
+        }
+        tmem_st16(tDP + c * 16, pk);
+        // dS^T row r, query columns 32c .. 32c+31 -> MN-major (query-contiguous)
+        // 128-byte swizzled layout: chunk (c / 2) of 64 queries, units 4(c%2)..+3.
+        const uint32_t base = aDS + (c >> 1) * C::kChunkBytes;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(base + sw128_offset(r, (c & 1) * 4 + u), pk[4 * u], pk[4 * u + 1],
+                       pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_dsready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_qempty[st]);
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+    // ---------------------------------------------------------- dV epilogue
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dkvdone, 0));
+      if (ok) {
+        tc_fence_after();
+        const uint32_t tDV = tmem + lane_off + C::kColDV;
+        const uint32_t aStage = smem_u32(sQ);  // free after the loop
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tDV + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+          const uint32_t base = aStage + (c >> 1) * C::kChunkBytes;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(base + sw128_offset(r, (c & 1) * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (r == 0) {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_store_3d(&tmDV, sQ + c * C::kChunkBytes, c * 64, j * kBlockN, bh);
+          bulk_commit_group();
+          bulk_wait_group0();
+        }
+      } else {
+        set_fail(ATTN_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    // ------------------------------------------------------------ dQ drain
+    const int r = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tDQ = tmem + lane_off + C::kColDQ;
+    bool ok = !abort_all;
+    for (int it = 0; it < nq && ok; ++it) {
+      const int i = i_first + it;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dqfull, it & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t acc[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tDQ + c * 32, acc[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) reg_fence(acc[c]);
+      tc_fence_before();
+      mbar_arrive(bar_dqfree);
+      float* dst = dqacc + ((size_t)bh * Npad + (size_t)i * kBlockM + r) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          red_add_v4(dst + c * 32 + e, __uint_as_float(acc[c][e]), __uint_as_float(acc[c][e + 1]),
+                     __uint_as_float(acc[c][e + 2]), __uint_as_float(acc[c][e + 3]));
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+    // ---------------------------------------------------------- dK epilogue
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dkvdone, 0));
+      if (ok) {
+        tc_fence_after();
+        const uint32_t tDK = tmem + lane_off + C::kColDK;
+        const uint32_t aStage = smem_u32(sDO);  // free after the loop
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tDK + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * scale,
+                                __uint_as_float(o[2 * e + 1]) * scale);
+          const uint32_t base = aStage + (c >> 1) * C::kChunkBytes;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(base + sw128_offset(r, (c & 1) * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (r == 0) {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_store_3d(&tmDK, sDO + c * C::kChunkBytes, c * 64, j * kBlockN, bh);
+          bulk_commit_group();
+          bulk_wait_group0();
+        }
+      } else {
+        set_fail(ATTN_ERR_TIMEOUT);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t preprocess_impl(const Problem& p, const void* o, const void* dout, const float* lse,
+                            const BwdWorkspace& ws, cudaStream_t stream) {
+  constexpr int kRows = 256 / (D / 8);
+  const int Npad = n_pad(p.N);
+  dim3 grid(ceil_div(Npad, kRows), p.B * p.H);
+  bwd_preprocess_kernel<D><<<grid, 256, 0, stream>>>(
+      static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, ws.lse2, ws.delta,
+      reinterpret_cast<float4*>(ws.dqacc), p.N, Npad);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dq_convert_impl(const Problem& p, const BwdWorkspace& ws, void* dq,
+                            cudaStream_t stream) {
+  const long long units = (long long)p.B * p.H * p.N * (D / 8);
+  const int blocks = (int)((units + 255) / 256);
+  bwd_dq_convert_kernel<D><<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws.dqacc),
+                                                       static_cast<uint4*>(dq), p.N, n_pad(p.N),
+                                                       p.scale, (int)units);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t main_impl(const Problem& p, const CUtensorMap* maps, const BwdWorkspace& ws,
+                      cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  auto kernel = bwd_main_kernel<D, CAUSAL>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int BH = p.B * p.H;
+  const int Npad = n_pad(p.N);
+  const int n_kt = Npad / kBlockN;
+  kernel<<<dim3(BH * n_kt), dim3(kThreads), C::kSmemBytes, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.lse2, ws.delta, ws.dqacc, BH, p.N,
+      Npad, p.scale, p.scale * 1.4426950408889634f);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess_bf16(const Problem& p, const void* o, const void* dout,
+                                       const float* lse, const BwdWorkspace& ws,
+                                       cudaStream_t stream) {
+  return p.d == 128 ? preprocess_impl<128>(p, o, dout, lse, ws, stream)
+                    : preprocess_impl<64>(p, o, dout, lse, ws, stream);
+}
+
+cudaError_t launch_bwd_dq_convert_bf16(const Problem& p, const BwdWorkspace& ws, void* dq,
+                                       cudaStream_t stream) {
+  return p.d == 128 ? dq_convert_impl<128>(p, ws, dq, stream)
+                    : dq_convert_impl<64>(p, ws, dq, stream);
+}
+
+cudaError_t launch_bwd_main_bf16(const Problem& p, const void* q, const void* k, const void* v,
+                                 const void* dout, void* dk, void* dv, const BwdWorkspace& ws,
+                                 cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  CUtensorMap maps[6];
+  const void* ptrs[6] = {q, k, v, dout, dk, dv};
+  for (int i = 0; i < 6; ++i)
+    if (!make_tmap_bhnd(&maps[i], ptrs[i], BH, p.N, p.d)) return cudaErrorInvalidValue;
+  if (p.d == 128)
+    return p.causal ? main_impl<128, true>(p, maps, ws, stream)
+                    : main_impl<128, false>(p, maps, ws, stream);
+  return p.causal ? main_impl<64, true>(p, maps, ws, stream)
+                  : main_impl<64, false>(p, maps, ws, stream);
+}
+
+cudaError_t read_and_clear_status_bwd(unsigned int* out, cudaStream_t stream) {
+  static const unsigned int zero = 0;
+  cudaError_t err = cudaMemcpyFromSymbolAsync(out, g_status_bwd, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+  if (err != cudaSuccess) return err;
+  err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return err;
+  err = cudaMemcpyToSymbolAsync(g_status_bwd, &zero, sizeof(unsigned int), 0,
+                                cudaMemcpyHostToDevice, stream);
+  if (err != cudaSuccess) return err;
+  return cudaStreamSynchronize(stream);
+}
+
+}  // namespace attn

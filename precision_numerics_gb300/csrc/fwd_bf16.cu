@@ -1,0 +1,410 @@
+// BF16 attention forward for sm_103a: TMA + tcgen05 (TMEM accumulators),
+// warp-specialised producer / MMA / softmax roles, FP32 online softmax.
+//
+// What is computed: O = softmax(scale Q K^T [+ causal mask]) V and the
+// natural-log LSE of each row ("Is Flash Attention Stable?", abstract:
+// Baseline Attention), evaluated blockwise as in "Why Low-Precision
+// Transformer Training Fails", Algorithm 1: Q is cut into 128-row blocks,
+// K and V into 128-row blocks; for each K/V block the row max m is updated,
+// P = exp(S - m) (P-bar in that paper's Figures 5 and 7), the row sum and
+// the partial output are rescaled by exp(m_old - m_new), and P V is
+// accumulated.  The softmax runs in FP32; P is rounded to BF16 (nearest
+// even) only as the operand of the P V product; the row sum accumulates the
+// FP32 values.
+//
+// CTA = 2 query tiles of 128 rows (256 rows of one (b, h)), 12 warps:
+//   warp 0      TMA producer (Q once; K_j, V_j through a shared-memory ring)
+//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
+//   warp 2      TMEM allocation owner
+//   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1; each
+//               thread owns one query row (one TMEM lane), so row max and
+//               row sum need no cross-thread reduction.
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
+// O_1 [256+d,256+2d).  P_t (BF16, two per 32-bit column) overwrites the
+// first 64 columns of S_t and is the A operand of the P V MMA.  The MMA
+// issue order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) lets the tensor pipe
+// work on one tile while the other tile's softmax runs.
+#include <math.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+static __device__ unsigned int g_status_fwd;
+
+namespace {
+
+constexpr int kThreads = 384;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kChunks = D / 64;          // 64-column (128-byte) chunks per row
+  static constexpr int kChunkBytes = 128 * 128;   // 128 rows x 128 bytes
+  static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x d BF16
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
+  // o_done[2], mma_final
+  static constexpr int kNumBars = 1 + 4 * kStages + 7;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM column of S_t and O_t.
+  static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+  static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * t; }
+};
+
+__device__ __forceinline__ void set_fail(unsigned int code) { atomicOr(&g_status_fwd, code); }
+
+// Number of K/V tiles the query tile starting at row q_first visits.
+__device__ __forceinline__ int kv_tiles_for(int q_first, int N, bool causal) {
+  if (q_first >= N) return 0;
+  if (!causal) return (N + kBlockN - 1) / kBlockN;
+  const int q_last = min(q_first + kBlockM - 1, N - 1);
+  return q_last / kBlockN + 1;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    float* __restrict__ lse, int BH, int N, int num_qt, float scale,
+                    float scale_log2) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Heaviest (largest causal) query tiles first.
+  const int L = blockIdx.x;
+  const int qt = num_qt - 1 - L / BH;
+  const int bh = L % BH;
+  const int q0 = qt * (2 * kBlockM);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* bar_q = bars;
+  uint64_t* bar_kfull = bars + 1;
+  uint64_t* bar_kempty = bar_kfull + C::kStages;
+  uint64_t* bar_vfull = bar_kempty + C::kStages;
+  uint64_t* bar_vempty = bar_vfull + C::kStages;
+  uint64_t* bar_sfull = bar_vempty + C::kStages;
+  uint64_t* bar_pfull = bar_sfull + 2;
+  uint64_t* bar_odone = bar_pfull + 2;
+  uint64_t* bar_final = bar_odone + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+
+  const int n0 = kv_tiles_for(q0, N, CAUSAL);
+  const int n1 = kv_tiles_for(q0 + kBlockM, N, CAUSAL);
+  const int nmax = max(n0, n1);
+
+  if (threadIdx.x == 0) {
+    s_abort = (smem_u32(smem) & 1023u) != 0;
+    if (s_abort) set_fail(ATTN_ERR_INVALID_ARG);
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_kfull[s], 1);
+      mbar_init(&bar_kempty[s], 1);
+      mbar_init(&bar_vfull[s], 1);
+      mbar_init(&bar_vempty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_sfull[t], 1);
+      mbar_init(&bar_pfull[t], 128);
+      mbar_init(&bar_odone[t], 1);
+    }
+    mbar_init(bar_final, 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool abort_all = s_abort != 0;
+
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (warp == 0 && lane == 0 && !abort_all) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, bar_q, c * 64,
+                      q0 + t * kBlockM, bh);
+      bool ok = true;
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < nmax; ++j) {
+        const int st = j % C::kStages;
+        const int use = j / C::kStages;
+        if (use > 0 && !mbar_wait(&bar_kempty[st], (use - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bar_kfull[st], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sK + st * C::kTileBytes + c * C::kChunkBytes, &tmK, &bar_kfull[st], c * 64,
+                      j * kBlockN, bh);
+        issued_k = j + 1;
+        if (use > 0 && !mbar_wait(&bar_vempty[st], (use - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bar_vfull[st], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sV + st * C::kTileBytes + c * C::kChunkBytes, &tmV, &bar_vfull[st], c * 64,
+                      j * kBlockN, bh);
+        issued_v = j + 1;
+      }
+      if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      mbar_wait(bar_q, 0);
+      for (int j = max(0, issued_k - C::kStages); j < issued_k; ++j)
+        mbar_wait(&bar_kfull[j % C::kStages], (j / C::kStages) & 1);
+      for (int j = max(0, issued_v - C::kStages); j < issued_v; ++j)
+        mbar_wait(&bar_vfull[j % C::kStages], (j / C::kStages) & 1);
+    } else if (warp == 1 && lane == 0 && !abort_all) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      const int n_t[2] = {n0, n1};
+      bool ok = mbar_wait(bar_q, 0);
+      auto issue_s = [&](int t, int st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(aQ + t * C::kTileBytes + off, 16, 1024);
+          const uint64_t b = sdesc_sw128(aK + st * C::kTileBytes + off, 16, 1024);
+          mma_ss(tmem + C::col_s(t), a, b, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int st, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(aV + st * C::kTileBytes + kk * 2048, C::kChunkBytes, 1024);
+          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, b, idesc_pv,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      if (ok && nmax > 0) {
+        ok = mbar_wait(&bar_kfull[0], 0);
+        tc_fence_after();
+        if (ok) {
+          for (int t = 0; t < 2; ++t)
+            if (n_t[t] > 0) {
+              issue_s(t, 0);
+              mma_commit(&bar_sfull[t]);
+            }
+        }
+      }
+      for (int j = 0; j < nmax && ok; ++j) {
+        const int st = j % C::kStages;
+        const int st1 = (j + 1) % C::kStages;
+        const bool has_next = j + 1 < nmax;
+        if (!mbar_wait(&bar_vfull[st], (j / C::kStages) & 1)) { ok = false; break; }
+        if (has_next && !mbar_wait(&bar_kfull[st1], ((j + 1) / C::kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          if (!mbar_wait(&bar_pfull[t], j & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(t, st, j > 0);
+          if (j + 1 < n_t[t]) {
+            issue_s(t, st1);
+            mma_commit(&bar_sfull[t]);
+          } else {
+            mma_commit(&bar_odone[t]);
+          }
+        }
+        mma_commit(&bar_vempty[st]);
+        mma_commit(&bar_kempty[st]);
+      }
+      if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+      // Every MMA this thread issued completes before TMEM is released.
+      mma_commit(bar_final);
+      mbar_wait(bar_final, 0);
+    }
+    __syncwarp();
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    // -------------------------------------------------------------- softmax
+    const int t = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::col_s(t);
+    const uint32_t tO = tmem + lane_off + C::col_o(t);
+    const int q_first = q0 + t * kBlockM;
+    const int qi = q_first + r;
+    const int n = abort_all ? 0 : (t == 0 ? n0 : n1);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_sfull[t], j & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence(s[c]);
+
+      const int kv0 = j * kBlockN;
+      if (kv0 + kBlockN > N || (CAUSAL && kv0 + kBlockN - 1 > q_first)) {
+        const int lim = (CAUSAL ? min(qi + 1, N) : N) - kv0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+      }
+      float mx = __uint_as_float(s[0][0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c >> 5][c & 31]));
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float neg_ms = -m_use * scale_log2;
+      const float alpha = ex2((m_run - m_use) * scale_log2);
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[c][2 * i]), scale_log2, neg_ms));
+          const float p1 = ex2(fmaf(__uint_as_float(s[c][2 * i + 1]), scale_log2, neg_ms));
+          sum0 += p0;
+          sum1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      // Rescale the partial output when any row max in this warp moved.
+      // PV(j-1) has completed: the commit that released S(j) covers it.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_pfull[t]);
+      m_run = m_new;
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+    if (n > 0 && ok) {
+      // ------------------------------------------------------------ epilogue
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_odone[t], 0));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint8_t* stage = sQ + t * C::kTileBytes;  // Q_t is no longer read
+        const uint32_t aStage = smem_u32(stage);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                __uint_as_float(o[2 * i + 1]) * inv_l);
+          const uint32_t base = aStage + (c >> 1) * C::kChunkBytes;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(base + sw128_offset(r, (c & 1) * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, 128);
+        if (r == 0) {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_store_3d(&tmO, stage + c * C::kChunkBytes, c * 64, q_first, bh);
+          bulk_commit_group();
+          bulk_wait_group0();
+        }
+        if (qi < N) {
+          const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
+          lse[(size_t)bh * N + qi] = m_fin * scale + logf(l_run);
+        }
+      } else {
+        set_fail(ATTN_ERR_TIMEOUT);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mo, float* lse,
+                            cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kernel = fwd_bf16_kernel<D, CAUSAL>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int BH = p.B * p.H;
+  const int num_qt = ceil_div(p.N, 2 * kBlockM);
+  const float scale_log2 = p.scale * 1.4426950408889634f;
+  kernel<<<dim3(BH * num_qt), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, mo, lse, BH, p.N,
+                                                                       num_qt, p.scale, scale_log2);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                            float* lse, cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_tmap_bhnd(&mq, q, BH, p.N, p.d) || !make_tmap_bhnd(&mk, k, BH, p.N, p.d) ||
+      !make_tmap_bhnd(&mv, v, BH, p.N, p.d) || !make_tmap_bhnd(&mo, o, BH, p.N, p.d))
+    return cudaErrorInvalidValue;
+  if (p.d == 128)
+    return p.causal ? launch_fwd_impl<128, true>(p, mq, mk, mv, mo, lse, stream)
+                    : launch_fwd_impl<128, false>(p, mq, mk, mv, mo, lse, stream);
+  return p.causal ? launch_fwd_impl<64, true>(p, mq, mk, mv, mo, lse, stream)
+                  : launch_fwd_impl<64, false>(p, mq, mk, mv, mo, lse, stream);
+}
+
+cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream) {
+  static const unsigned int zero = 0;
+  cudaError_t err = cudaMemcpyFromSymbolAsync(out, g_status_fwd, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+  if (err != cudaSuccess) return err;
+  err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return err;
+  err = cudaMemcpyToSymbolAsync(g_status_fwd, &zero, sizeof(unsigned int), 0,
+                                cudaMemcpyHostToDevice, stream);
+  if (err != cudaSuccess) return err;
+  return cudaStreamSynchronize(stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,103 @@
+"""The C ABI: the library loads, exports what include/attn.h declares, and its
+host-side argument checks behave (CPU only; no kernel is launched)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from precision_numerics_gb300 import attn, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return attn.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(attn.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True).stdout
+    names = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert {n for n in names if n.startswith("attn_")} == set(declared_functions())
+
+
+def test_status_strings(lib):
+    assert lib.attn_status_string(0).decode() == "ATTN_OK"
+    assert b"TIMEOUT" in lib.attn_status_string(4)
+    assert lib.attn_version() >= 100
+
+
+def test_workspace_bytes(lib):
+    # lse2 + delta: B*H*Npad floats each (256-byte aligned), dQ accumulator B*H*Npad*d floats.
+    def expect(B, H, N, d):
+        npad = -(-N // 128) * 128
+        a = -(-(B * H * npad * 4) // 256) * 256
+        c = -(-(B * H * npad * d * 4) // 256) * 256
+        return 2 * a + c
+    for shape in [(1, 1, 1, 64), (1, 32, 4096, 128), (8, 12, 1024, 64), (2, 3, 129, 128)]:
+        assert lib.attn_bwd_workspace_bytes(*shape, 0) == expect(*shape)
+    assert lib.attn_bwd_workspace_bytes(1, 1, 128, 96, 0) == 0
+    assert lib.attn_bwd_workspace_bytes(1, 1, 0, 64, 0) == 0
+
+
+def _fwd(lib, **kw):
+    a = dict(q=None, k=None, v=None, o=None, lse=None, B=1, H=1, N=128, d=64, scale=0.125,
+             causal=0, dt=0)
+    a.update(kw)
+    r = lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                     ctypes.c_float(a["scale"]), a["causal"], a["dt"], None)
+    return r, lib.attn_last_error().decode()
+
+
+def test_argument_errors_are_reported_before_any_launch(lib):
+    r, msg = _fwd(lib, d=96)
+    assert r == attn.ATTN_ERR_UNSUPPORTED and "96" in msg
+    r, _ = _fwd(lib, N=0)
+    assert r == attn.ATTN_ERR_INVALID_ARG
+    r, msg = _fwd(lib, scale=float("nan"))
+    assert r == attn.ATTN_ERR_INVALID_ARG and "scale" in msg
+    r, _ = _fwd(lib, scale=-1.0)
+    assert r == attn.ATTN_ERR_INVALID_ARG
+    r, _ = _fwd(lib, dt=7)
+    assert r == attn.ATTN_ERR_INVALID_ARG
+    r, _ = _fwd(lib, B=65536, H=65536)
+    assert r == attn.ATTN_ERR_INVALID_ARG
+    r, msg = _fwd(lib)  # null pointers
+    assert r == attn.ATTN_ERR_INVALID_ARG and "NULL" in msg
+    r, msg = _fwd(lib, q=16 * 1001 + 8, k=16, v=16, o=16, lse=16)
+    assert r == attn.ATTN_ERR_INVALID_ARG and "aligned" in msg
+
+
+def test_selftest_limit_is_checked(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_wait_timeout(2 * 10**9, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        attn.load_library(str(tmp_path / "libattn.so"))

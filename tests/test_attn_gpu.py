@@ -1,0 +1,204 @@
+"""Parity of the CUDA path (through the C ABI) with the FP64 oracle.
+
+Tolerances: BF16 -- O max-abs 2e-2 and mean-abs 2e-3, LSE max-abs 1e-3,
+dQ/dK/dV relative L2 1e-2; FP32 reference mode -- relative 1e-5
+(relative L2 and max-abs over max |ref|), LSE max-abs 1e-5 * max(1, |LSE|).
+Inputs are the seeded generator's values; the oracle sees exactly the values
+the GPU sees, widened to FP64.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from precision_numerics_gb300 import inputs
+from precision_numerics_gb300.deviation import deviation
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def A(cuda_device):
+    from precision_numerics_gb300 import attn, build
+    build.build()
+    attn.load_library()
+    return attn
+
+
+def _dev(x, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _widen(x, dtype):
+    return inputs.bf16_bits_to_f32(x) if dtype == "bf16" else x
+
+
+def _run(A, x, dtype, scale, causal, backward=True):
+    t = {k: _dev(v, dtype) for k, v in x.items()}
+    o, lse = A.attn_fwd(t["q"], t["k"], t["v"], scale=scale, causal=causal)
+    out = {"o": o, "lse": lse}
+    if backward:
+        dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=scale, causal=causal)
+        out.update(dq=dq, dk=dk, dv=dv)
+    A.attn_check_status()
+    return {k: _host(v) for k, v in out.items()}
+
+
+def _oracle(x, dtype, scale, causal, backward=True):
+    f = {k: _widen(v, dtype) for k, v in x.items()}
+    o, lse = oracle.forward_bhnd(f["q"], f["k"], f["v"], scale, causal)
+    ref = {"o": o, "lse": lse}
+    if backward:
+        ref["dq"], ref["dk"], ref["dv"] = oracle.backward_bhnd(f["q"], f["k"], f["v"], f["do"],
+                                                              scale, causal)
+    return ref
+
+
+def _assert_bf16(got, ref, backward=True, tag=""):
+    e = deviation(got["o"], ref["o"])
+    assert e["max_abs"] <= 2e-2 and e["mean_abs"] <= 2e-3, (tag, "o", e)
+    e = deviation(got["lse"], ref["lse"])
+    assert e["max_abs"] <= 1e-3, (tag, "lse", e)
+    if backward:
+        for name in ("dq", "dk", "dv"):
+            e = deviation(got[name], ref[name])
+            assert e["rel_l2"] <= 1e-2, (tag, name, e)
+
+
+def _assert_fp32(got, ref, backward=True, tag=""):
+    for name in ("o",) + (("dq", "dk", "dv") if backward else ()):
+        e = deviation(got[name], ref[name])
+        assert e["rel_l2"] <= 1e-5 and e["max_rel"] <= 1e-5, (tag, name, e)
+    lse_tol = 1e-5 * max(1.0, float(np.abs(ref["lse"]).max()))
+    assert deviation(got["lse"], ref["lse"])["max_abs"] <= lse_tol, (tag, "lse")
+
+
+SHAPES = [(1, 2, 128, 64), (1, 1, 1, 64), (1, 2, 17, 128), (2, 1, 129, 64), (1, 2, 256, 128),
+          (1, 1, 300, 128), (2, 2, 511, 64), (1, 2, 640, 128)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_fp32_reference_mode(A, shape, causal):
+    B, H, N, d = shape
+    x = inputs.random_qkv(1, B, H, N, d, dtype="fp32")
+    scale = 1.0 / math.sqrt(d)
+    _assert_fp32(_run(A, x, "fp32", scale, causal), _oracle(x, "fp32", scale, causal), tag=shape)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES + [(1, 1, 1000, 64), (1, 1, 1024, 128)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_forward_backward(A, shape, causal):
+    B, H, N, d = shape
+    x = inputs.random_qkv(2, B, H, N, d)
+    scale = 1.0 / math.sqrt(d)
+    _assert_bf16(_run(A, x, "bf16", scale, causal), _oracle(x, "bf16", scale, causal), tag=shape)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_small_workload_forward(A, dtype):
+    """B1 H2 N128 d64 non-causal, scale 1/sqrt(d), FP32 and BF16 inputs."""
+    w = inputs.WORKLOADS["small"]
+    x = inputs.make_inputs(w, seed=0, dtype=dtype)
+    got = _run(A, x, dtype, w.scale, w.causal, backward=False)
+    ref = _oracle(x, dtype, w.scale, w.causal, backward=False)
+    (_assert_fp32 if dtype == "fp32" else _assert_bf16)(got, ref, backward=False)
+
+
+def test_single_key_closed_form(A):
+    """N = 1: O = V[0] exactly (one key with weight 1)."""
+    x = inputs.random_qkv(3, 2, 3, 1, 128)
+    got = _run(A, x, "bf16", 0.1, False, backward=False)
+    v = inputs.bf16_bits_to_f32(x["v"]).astype(np.float64)
+    np.testing.assert_array_equal(got["o"], v)
+
+
+def test_causal_row0_is_v0(A):
+    x = inputs.random_qkv(4, 1, 2, 256, 64)
+    got = _run(A, x, "bf16", 0.125, True, backward=False)
+    v = inputs.bf16_bits_to_f32(x["v"]).astype(np.float64)
+    np.testing.assert_array_equal(got["o"][:, :, 0], v[:, :, 0])
+
+
+def test_forward_is_deterministic(A):
+    x = inputs.random_qkv(5, 1, 4, 700, 128)
+    t = {k: _dev(v, "bf16") for k, v in x.items()}
+    o1, l1 = A.attn_fwd(t["q"], t["k"], t["v"], causal=True)
+    o2, l2 = A.attn_fwd(t["q"], t["k"], t["v"], causal=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_backward_phases_equal_attn_bwd(A):
+    B, H, N, d = 1, 2, 300, 128
+    x = inputs.random_qkv(6, B, H, N, d)
+    t = {k: _dev(v, "bf16") for k, v in x.items()}
+    o, lse = A.attn_fwd(t["q"], t["k"], t["v"], causal=True)
+    dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=True)
+    ws = torch.empty(A.attn_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    dq2, dk2, dv2 = (torch.empty_like(o) for _ in range(3))
+    A.attn_bwd_preprocess(o, lse, t["do"], ws)
+    A.attn_bwd_main(t["q"], t["k"], t["v"], t["do"], dk2, dv2, ws, causal=True)
+    A.attn_bwd_dq_convert(dq2, ws)
+    A.attn_check_status()
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert (dq.float() - dq2.float()).abs().max().item() <= 2e-2 * dq.float().abs().max().item()
+
+
+@pytest.mark.parametrize("N,d,causal", [(129, 128, True), (300, 64, False), (1, 128, False)])
+def test_outputs_leave_guard_bands_untouched(A, N, d, causal):
+    """Outputs sit inside larger buffers whose tails hold a sentinel (all-ones bits)."""
+    B, H, guard = 1, 3, 4096
+    x = inputs.random_qkv(7, B, H, N, d)
+    t = {k: _dev(v, "bf16") for k, v in x.items()}
+    n = B * H * N * d
+
+    def guarded(numel, dtype):
+        buf = torch.empty(numel + guard, dtype=dtype, device="cuda")
+        buf.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).fill_(-1)
+        return buf
+
+    ob, lb = guarded(n, torch.bfloat16), guarded(B * H * N, torch.float32)
+    o = ob[:n].view(B, H, N, d)
+    lse = lb[:B * H * N].view(B, H, N)
+    A.attn_fwd(t["q"], t["k"], t["v"], causal=causal, o=o, lse=lse)
+    gb = [guarded(n, torch.bfloat16) for _ in range(3)]
+    A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=causal,
+               dq=gb[0][:n].view(B, H, N, d), dk=gb[1][:n].view(B, H, N, d),
+               dv=gb[2][:n].view(B, H, N, d))
+    A.attn_check_status()
+    for buf in [ob, *gb]:
+        assert bool((buf[n:].view(torch.int16) == -1).all())
+    assert bool((lb[B * H * N:].view(torch.int32) == -1).all())
+    assert bool(torch.isfinite(o.float()).all())
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(A):
+    A.attn_check_status()
+    A.attn_selftest_wait_timeout(2_000_000)  # 2 ms
+    with pytest.raises(A.AttnError) as info:
+        A.attn_check_status()
+    assert info.value.status == A.ATTN_ERR_TIMEOUT
+    A.attn_check_status()  # cleared
+    x = inputs.random_qkv(8, 1, 1, 128, 64)
+    got = _run(A, x, "bf16", 0.125, False, backward=False)
+    _assert_bf16(got, _oracle(x, "bf16", 0.125, False, backward=False), backward=False)
+
+
+def test_rejects_host_memory(A):
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device="cuda")
+    lib = A.load_library()
+    host = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16).pin_memory()
+    lse = torch.empty(1, 1, 128, device="cuda")
+    r = lib.attn_fwd(host.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), lse.data_ptr(),
+                     1, 1, 128, 64, 0.125, 0, 0, None)
+    assert r == A.ATTN_ERR_INVALID_ARG

@@ -1,0 +1,75 @@
+"""Full-size workloads on the GPU, checked on sampled heads against the oracle.
+
+Each workload runs at its full size in the launch configuration the bench
+times (whole [B, H, N, d] tensors, one forward and one backward call); the
+FP64 oracle then recomputes a few (b, h) heads in full and the GPU values of
+those heads must meet the BF16 tolerances (O max-abs 2e-2, mean-abs 2e-3,
+LSE max-abs 1e-3, dQ/dK/dV relative L2 1e-2).  Every head is checked for
+finiteness.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from precision_numerics_gb300 import inputs
+from precision_numerics_gb300.deviation import deviation
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def A(cuda_device):
+    from precision_numerics_gb300 import attn, build
+    build.build()
+    return attn
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _check(A, w, x, heads):
+    t = {k: _dev(v) for k, v in x.items()}
+    o, lse = A.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
+    dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale,
+                            causal=w.causal)
+    A.attn_check_status()
+    for name, g in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert bool(torch.isfinite(g.float()).all()), name
+    bh = w.B * w.H
+    flat = {k: v.reshape(bh, w.N, w.d) for k, v in x.items()}
+    got = {k: g.reshape(bh, w.N, -1) for k, g in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv))}
+    got["lse"] = lse.reshape(bh, w.N)
+    for h in heads:
+        f = {k: inputs.bf16_bits_to_f32(v[h]) for k, v in flat.items()}
+        o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+        refs = dict(zip(("dq", "dk", "dv"),
+                        oracle.backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)))
+        refs.update(o=o_ref, lse=lse_ref)
+        dev = {k: deviation(got[k][h].float().cpu().numpy(), refs[k]) for k in refs}
+        assert dev["o"]["max_abs"] <= 2e-2 and dev["o"]["mean_abs"] <= 2e-3, (h, dev["o"])
+        assert dev["lse"]["max_abs"] <= 1e-3, (h, dev["lse"])
+        for k in ("dq", "dk", "dv"):
+            assert dev[k]["rel_l2"] <= 1e-2, (h, k, dev[k])
+
+
+def test_gpt2_shape(A):
+    w = inputs.WORKLOADS["gpt2"]
+    _check(A, w, inputs.make_inputs(w, seed=0), heads=[0, w.B * w.H - 1])
+
+
+def test_llama7b_shape(A):
+    w = inputs.WORKLOADS["llama7b"]
+    _check(A, w, inputs.make_inputs(w, seed=0), heads=[0, 17, w.B * w.H - 1])
+
+
+@pytest.mark.parametrize("sigma", [1.0, 4.0, 16.0])
+def test_lowrank_shape(A, sigma):
+    w = inputs.WORKLOADS["lowrank"]
+    _check(A, w, inputs.make_inputs(w, seed=0, sigma=sigma), heads=[0, w.B * w.H - 1])
+
+
+def test_longseq_shape(A):
+    w = inputs.WORKLOADS["longseq"]
+    _check(A, w, inputs.make_inputs(w, seed=0), heads=[w.B * w.H - 1])
