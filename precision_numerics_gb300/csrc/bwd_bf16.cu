@@ -130,8 +130,8 @@ struct BwdCfg {
   static constexpr int kOffDelta = kOffLse + 2 * 512;  // 2 stages x 128 FP32
   static constexpr int kOffBar = kOffDelta + 2 * 512;
   // kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_ready, ds_ready,
-  // dq_full, dq_free, dkv_done, mma_final
-  static constexpr int kNumBars = 13;
+  // dq_full, dq_free, dkv_done, mma_final, epi_dv, epi_dk
+  static constexpr int kNumBars = 15;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static constexpr uint32_t kColDV = 0;
   static constexpr uint32_t kColDK = D;
@@ -152,7 +152,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float scale_log2) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -176,11 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_dqfree = bars + 10;
   uint64_t* bar_dkvdone = bars + 11;
   uint64_t* bar_final = bars + 12;
+  uint64_t* bar_epi_dv = bars + 13;
+  uint64_t* bar_epi_dk = bars + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
-    s_abort = (smem_u32(smem) & 1023u) != 0;
-    if (s_abort) set_fail(ATTN_ERR_INVALID_ARG);
+    *s_abort = (smem_u32(smem) & 1023u) != 0;
+    if (*s_abort) set_fail(ATTN_ERR_INVALID_ARG);
     mbar_init(bar_kv, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_qfull[s], 1);
@@ -194,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_dqfree, 128);
     mbar_init(bar_dkvdone, 1);
     mbar_init(bar_final, 1);
+    mbar_init(bar_epi_dv, 128);
+    mbar_init(bar_epi_dk, 128);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool abort_all = s_abort != 0;
+  const bool abort_all = *s_abort != 0;
 
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
@@ -428,12 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pk[4 * u + 2], pk[4 * u + 3]);
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        mbar_arrive(bar_epi_dv);
         if (r == 0) {
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_store_3d(&tmDV, sQ + c * C::kChunkBytes, c * 64, j * kBlockN, bh);
-          bulk_commit_group();
-          bulk_wait_group0();
+          if (mbar_wait(bar_epi_dv, 0)) {
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_store_3d(&tmDV, sQ + c * C::kChunkBytes, c * 64, j * kBlockN, bh);
+            bulk_commit_group();
+            bulk_wait_group0();
+          } else {
+            set_fail(ATTN_ERR_TIMEOUT);
+          }
         }
       } else {
         set_fail(ATTN_ERR_TIMEOUT);
@@ -493,12 +501,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pk[4 * u + 2], pk[4 * u + 3]);
         }
         fence_proxy_async_smem();
-        named_bar_sync(2, 128);
+        mbar_arrive(bar_epi_dk);
         if (r == 0) {
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_store_3d(&tmDK, sDO + c * C::kChunkBytes, c * 64, j * kBlockN, bh);
-          bulk_commit_group();
-          bulk_wait_group0();
+          if (mbar_wait(bar_epi_dk, 0)) {
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_store_3d(&tmDK, sDO + c * C::kChunkBytes, c * 64, j * kBlockN, bh);
+            bulk_commit_group();
+            bulk_wait_group0();
+          } else {
+            set_fail(ATTN_ERR_TIMEOUT);
+          }
         }
       } else {
         set_fail(ATTN_ERR_TIMEOUT);

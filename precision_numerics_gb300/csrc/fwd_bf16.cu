@@ -48,8 +48,8 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-  // o_done[2], mma_final
-  static constexpr int kNumBars = 1 + 4 * kStages + 7;
+  // o_done[2], epi[2], mma_final
+  static constexpr int kNumBars = 1 + 4 * kStages + 9;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static constexpr uint32_t kTmemCols = 512;
   // TMEM column of S_t and O_t.
@@ -75,7 +75,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float scale_log2) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -95,16 +94,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_sfull = bar_vempty + C::kStages;
   uint64_t* bar_pfull = bar_sfull + 2;
   uint64_t* bar_odone = bar_pfull + 2;
-  uint64_t* bar_final = bar_odone + 2;
+  uint64_t* bar_epi = bar_odone + 2;
+  uint64_t* bar_final = bar_epi + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int n0 = kv_tiles_for(q0, N, CAUSAL);
   const int n1 = kv_tiles_for(q0 + kBlockM, N, CAUSAL);
   const int nmax = max(n0, n1);
 
   if (threadIdx.x == 0) {
-    s_abort = (smem_u32(smem) & 1023u) != 0;
-    if (s_abort) set_fail(ATTN_ERR_INVALID_ARG);
+    *s_abort = (smem_u32(smem) & 1023u) != 0;
+    if (*s_abort) set_fail(ATTN_ERR_INVALID_ARG);
     mbar_init(bar_q, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bar_kfull[s], 1);
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_sfull[t], 1);
       mbar_init(&bar_pfull[t], 128);
       mbar_init(&bar_odone[t], 1);
+      mbar_init(&bar_epi[t], 128);
     }
     mbar_init(bar_final, 1);
     fence_mbar_init();
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool abort_all = s_abort != 0;
+  const bool abort_all = *s_abort != 0;
 
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sK = smem + C::kOffK;
@@ -336,12 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pk[4 * u + 2], pk[4 * u + 3]);
         }
         fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
+        mbar_arrive(&bar_epi[t]);
         if (r == 0) {
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_store_3d(&tmO, stage + c * C::kChunkBytes, c * 64, q_first, bh);
-          bulk_commit_group();
-          bulk_wait_group0();
+          if (mbar_wait(&bar_epi[t], 0)) {
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_store_3d(&tmO, stage + c * C::kChunkBytes, c * 64, q_first, bh);
+            bulk_commit_group();
+            bulk_wait_group0();
+          } else {
+            set_fail(ATTN_ERR_TIMEOUT);
+          }
         }
         if (qi < N) {
           const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
