@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the BF16 attention hot path (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama7b] [--deviation]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+attn_fwd (O, LSE) then the backward (preprocess, main kernel, dQ conversion).
+The default workload is B1 H32 N4096 d128, causal, BF16 (the Llama-2-7B-shaped
+case the target is quoted on).  FLOPs are counted as 4*B*H*N^2*d for the
+forward (halved when causal) and 2.5x that for the backward.
+
+Rank 0 prints ONE JSON line.  `value` is whole-job TFLOP/s with inputs
+resident in HBM; `e2e` is the same metric measured through the Python API
+with pinned host buffers (host->device copies of Q, K, V, dO and
+device->host copies of O, LSE, dQ, dK, dV inside the timed region);
+`roofline` describes the dominant kernel (the backward main kernel) timed
+with CUDA events on its stream; `cpu_baseline` is the FP64 oracle timed on
+the host cores on a bounded sample.  `--impl reference` times that oracle
+as the reference arm instead.  Under torchrun every rank runs its own full
+workload (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from precision_numerics_gb300 import inputs  # noqa: E402
+
+METRIC = "BF16 attention fwd/bwd TFLOP/s on 1 GB300, % of tensor peak; max err vs FP64"
+UNIT = "TFLOP/s"
+DOMINANT = "bwd_main_kernel"
+DOMINANT_SRC = os.path.join(ROOT, "precision_numerics_gb300", "csrc", "bwd_bf16.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "bwd_main_kernel_llama7b.md")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:  # noqa: BLE001 - fall back to the recorded fallback figures
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, float("inf"))
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if len(win) < 3:
+            win = self.samples
+        reasons = sorted({n for s in win for n, flag in zip(self.NAMES, s[3]) if flag == "Active"})
+        return {"sm_mhz": statistics.median(s[1] for s in win),
+                "sm_max_mhz": max(s[2] for s in win), "reasons": reasons, "samples": len(win)}
+
+
+# ---------------------------------------------------------------------------
+# roofline traffic from the committed ncu summary (null if the kernel changed)
+# ---------------------------------------------------------------------------
+def _source_sha():
+    with open(DOMINANT_SRC, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()
+
+
+def _traffic_per_launch(workload: str):
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_w = re.search(r"workload:\s*(\w+)", text)
+    if not (m_b and m_s and m_w) or m_s.group(1) != _source_sha() or m_w.group(1) != workload:
+        return None
+    return float(m_b.group(1))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def _oracle_head_step(w, x, head):
+    import oracle
+    f = {k: inputs.bf16_bits_to_f32(v.reshape(w.B * w.H, w.N, w.d)[head]) for k, v in x.items()}
+    oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+    oracle.backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)
+
+
+def _head_flops(w):
+    return (w.fwd_flops() + w.bwd_flops()) / (w.B * w.H)
+
+
+def _cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, x, budget_s=12.0):
+    """Time the oracle on whole heads (forward + backward) until ~budget_s."""
+    t0 = time.perf_counter()
+    heads = 0
+    while True:
+        _oracle_head_step(w, x, heads % (w.B * w.H))
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s or heads >= w.B * w.H:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": heads * _head_flops(w) / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(),
+            "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} (b,h) heads of {w.name}, FP64 forward+backward, "
+                      f"{dt:.1f} s; throughput scales linearly with heads"}
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    x = inputs.make_inputs(w, seed=0, heads=None)
+    for s in range(args.warmup):
+        _oracle_head_step(w, x, s % (w.B * w.H))
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        _oracle_head_step(w, x, s % (w.B * w.H))
+    dt = time.perf_counter() - t0
+    value = args.steps * _head_flops(w) / dt / 1e12
+    sample = f"each step = 1 of {w.B * w.H} (b,h) heads of {w.name}, FP64 forward+backward"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": _config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    return {"workload": f"{w.name}: B{w.B} H{w.H} N{w.N} d{w.d} "
+                        f"{'causal' if w.causal else 'non-causal'} BF16 forward+backward",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
+            "l2": "inputs larger than L2 (Q,K,V,O,dO,dQ,dK,dV and the FP32 dQ accumulator "
+                  f"are {(8 * 2 + 4) * w.B * w.H * w.N * w.d / 2**20:.0f} MiB per step vs 129 MB L2)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from precision_numerics_gb300 import attn, build
+    from precision_numerics_gb300.deviation import deviation
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    attn.load_library()
+
+    x = inputs.make_inputs(w, seed=rank)
+    host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+            for k, v in x.items()}
+    t = {k: v.to(dev) for k, v in host.items()}
+    B, H, N, d = w.B, w.H, w.N, w.d
+    o = torch.empty_like(t["q"])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(t["q"]) for _ in range(3))
+    ws = torch.empty(attn.attn_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    kernels_per_step = 4  # forward, backward preprocess, backward main, dQ conversion
+
+    def step(ev=None):
+        attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal, o=o, lse=lse)
+        attn.attn_bwd_preprocess(o, lse, t["do"], ws)
+        if ev is not None:
+            ev[0].record(stream)
+        attn.attn_bwd_main(t["q"], t["k"], t["v"], t["do"], dk, dv, ws, scale=w.scale,
+                           causal=w.causal)
+        if ev is not None:
+            ev[1].record(stream)
+        attn.attn_bwd_dq_convert(dq, ws, scale=w.scale)
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    for _ in range(args.warmup):
+        step()
+    attn.attn_check_status()
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark()
+    start.record(stream)
+    for s in range(args.steps):
+        step(events[s])
+    end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    main_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
+    attn.attn_check_status()
+
+    # End-to-end through the public API with pinned host buffers.
+    out_host = {k: torch.empty_like(host["q"]).pin_memory() for k in ("o", "dq", "dk", "dv")}
+    out_host["lse"] = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        t2 = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        o_, lse_ = attn.attn_fwd(t2["q"], t2["k"], t2["v"], scale=w.scale, causal=w.causal)
+        dq_, dk_, dv_ = attn.attn_bwd(t2["q"], t2["k"], t2["v"], o_, lse_, t2["do"], scale=w.scale,
+                                      causal=w.causal, workspace=ws)
+        for k_, v_ in (("o", o_), ("lse", lse_), ("dq", dq_), ("dk", dk_), ("dv", dv_)):
+            out_host[k_].copy_(v_, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    e2e_steps = max(1, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    attn.attn_check_status()
+    sampler.stop()
+
+    # Max over ranks.
+    if world > 1:
+        tt = torch.tensor([elapsed_ms, main_ms, e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms, main_ms, e2e_ms = (float(v) for v in tt.tolist())
+
+    if rank == 0:
+        peaks = _peaks()
+        step_flops = w.fwd_flops() + w.bwd_flops()
+        ms_per_step = elapsed_ms / args.steps
+        value = world * step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+        achieved = w.bwd_flops() / (main_ms * 1e-3) / 1e12
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+
+        # Max error vs FP64 on a sampled head (head 0) of the timed outputs.
+        import oracle
+        f = {k: inputs.bf16_bits_to_f32(v.reshape(B * H, N, d)[0]) for k, v in x.items()}
+        o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+        g_ref = oracle.backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)
+        err = {"o": deviation(o.reshape(B * H, N, d)[0].float().cpu().numpy(), o_ref),
+               "lse": deviation(lse.reshape(B * H, N)[0].cpu().numpy(), lse_ref)}
+        for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), g_ref):
+            err[name] = deviation(g.reshape(B * H, N, d)[0].float().cpu().numpy(), r)
+
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) inputs, generated on the host)",
+            "config": _config(w),
+            "pct_of_peak": 100.0 * (value / world) / peaks["bf16"],
+            "fwd_tflops": None, "bwd_main_tflops": achieved,
+            "max_err_vs_fp64": {"o_max_abs": err["o"]["max_abs"], "o_mean_abs": err["o"]["mean_abs"],
+                                "o_signed_mean": err["o"]["signed_mean"],
+                                "lse_max_abs": err["lse"]["max_abs"],
+                                "dq_rel_l2": err["dq"]["rel_l2"], "dk_rel_l2": err["dk"]["rel_l2"],
+                                "dv_rel_l2": err["dv"]["rel_l2"], "sample": "head (b,h)=(0,0)"},
+            "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
+                         "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16"],
+                         "frac_of_sustained": achieved / peaks["bf16_sustained"],
+                         "peak_source": f"{peaks['source']} bf16 burst",
+                         "traffic": _traffic_per_launch(w.name),
+                         "algorithmic": "2.5 * 4*B*H*N^2*d/2 FLOP per launch (5 matmuls)"},
+            "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": sampler.summary(),
+        }
+        line["fwd_tflops"] = _fwd_only_tflops(attn, t, o, lse, w, stream, torch)
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, x)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def _fwd_only_tflops(attn, t, o, lse, w, stream, torch, reps=20):
+    """Forward-only throughput (after the timed region; reported, not the headline)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal, o=o, lse=lse)
+    e0.record(stream)
+    for _ in range(reps):
+        attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal, o=o, lse=lse)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return w.fwd_flops() * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
+# deviation report (GPU vs FP64, next to naive BF16 attention vs FP64)
+# ---------------------------------------------------------------------------
+def run_deviation(args):
+    import torch
+
+    import oracle
+    from precision_numerics_gb300 import attn, build
+    from precision_numerics_gb300.deviation import deviation
+
+    build.build()
+    cases = [("small", None), ("gpt2", None), ("llama7b", None), ("lowrank", 1.0),
+             ("lowrank", 4.0), ("lowrank", 16.0), ("longseq", None)]
+    for name, sigma in cases:
+        w = inputs.WORKLOADS[name]
+        x = inputs.make_inputs(w, seed=0, sigma=sigma)
+        t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in x.items()}
+        o, lse = attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
+        g = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale, causal=w.causal)
+        attn.attn_check_status()
+        head = 0
+        f = {k: inputs.bf16_bits_to_f32(v.reshape(w.B * w.H, w.N, w.d)[head]) for k, v in x.items()}
+        o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+        g_ref = oracle.backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)
+        o_nv, lse_nv = oracle.naive_bf16_forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+        g_nv = oracle.naive_bf16_backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)
+        gpu = {"o": o, "lse": lse, "dq": g[0], "dk": g[1], "dv": g[2]}
+        ref = {"o": o_ref, "lse": lse_ref, "dq": g_ref[0], "dk": g_ref[1], "dv": g_ref[2]}
+        naive = {"o": o_nv, "lse": lse_nv, "dq": g_nv[0], "dk": g_nv[1], "dv": g_nv[2]}
+        rep = {"workload": name, "sigma": sigma, "head": head, "tiled_gpu": {}, "naive_bf16": {}}
+        for k in ref:
+            gv = gpu[k].reshape(w.B * w.H, *gpu[k].shape[2:])[head].float().cpu().numpy()
+            rep["tiled_gpu"][k] = deviation(gv, ref[k])
+            rep["naive_bf16"][k] = deviation(naive[k], ref[k])
+        print(json.dumps(rep), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama7b", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--deviation", action="store_true",
+                    help="print the numeric-deviation report instead of the bench line")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.deviation:
+        return run_deviation(args)
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
