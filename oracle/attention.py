@@ -18,7 +18,9 @@ What it computes, and where that is defined:
 * Backward -- the analytic gradient of that definition for a given dO:
   dV = P^T dO, dP = dO V^T, delta_i = rowsum(dO o O)_i ("Why Low-Precision
   Transformer Training Fails", Figures 3 and 5: delta = rowsum(dO o O)),
-  dS = P o (dP - delta), dQ = scale dS K, dK = scale dS^T Q.
+  dS = P o (dP - delta), dQ = scale dS K, dK = scale dS^T Q.  Optionally
+  delta is formed from a supplied (e.g. BF16-rounded) O instead, as in that
+  paper's Figure 3 (delta_lp = rowsum(dO o O_lp)).
 * The naive BF16 comparator -- "Baseline Attention at BF16" of "Is Flash
   Attention Stable?": materialised scores and probabilities, each matrix
   product accumulated in FP32 and rounded to BF16 (round to nearest even)
@@ -93,14 +95,20 @@ def delta(do, o):
     return (np.asarray(do, dtype=np.float64) * np.asarray(o, dtype=np.float64)).sum(axis=1)
 
 
-def backward(q, k, v, do, scale, causal):
-    """dQ, dK, dV of L = sum(dO o O) for O = forward(q, k, v), single head."""
+def backward(q, k, v, do, scale, causal, o_for_delta=None):
+    """dQ, dK, dV of L = sum(dO o O) for O = forward(q, k, v), single head.
+
+    With `o_for_delta` given, delta is taken as rowsum(dO o o_for_delta)
+    instead of from the exact O: the substitution of "Why Low-Precision
+    Transformer Training Fails", Figure 3, where delta_lp = rowsum(dO o O_lp)
+    is formed from a low-precision O.  Everything else stays exact.
+    """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     do = np.asarray(do, dtype=np.float64)
     p, _, _ = probabilities(q, k, scale, causal)
-    o = p @ v
+    o = p @ v if o_for_delta is None else np.asarray(o_for_delta, dtype=np.float64)
     dv = p.T @ do
     dp = do @ v.T
     ds = p * (dp - delta(do, o)[:, None])

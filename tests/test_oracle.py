@@ -126,6 +126,26 @@ def test_delta_identity():
     np.testing.assert_allclose((p * dp).sum(axis=1), oracle.delta(do, o), rtol=1e-12, atol=1e-12)
 
 
+def test_delta_from_supplied_o():
+    """delta from a supplied O: with the exact O nothing changes; with O + E the
+    gradients move by the closed form dS' - dS = -P o (rowsum(dO o E))."""
+    n, d, scale = 9, 4, 0.7
+    q, k, v, do = (_rand(24 + s, n, d) for s in range(4))
+    for causal in (False, True):
+        p, _, _ = oracle.probabilities(q, k, scale, causal)
+        o = p @ v
+        g0 = oracle.backward(q, k, v, do, scale, causal)
+        g1 = oracle.backward(q, k, v, do, scale, causal, o_for_delta=o)
+        for a, b in zip(g0, g1):
+            np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+        e = 1e-3 * _rand(28, n, d)
+        g2 = oracle.backward(q, k, v, do, scale, causal, o_for_delta=o + e)
+        dds = -p * (do * e).sum(axis=1)[:, None]
+        np.testing.assert_allclose(g2[0] - g0[0], scale * dds @ k, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(g2[1] - g0[1], scale * dds.T @ q, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(g2[2], g0[2], rtol=0, atol=0)
+
+
 # ---------------------------------------------------------------- library routines
 
 @pytest.mark.parametrize("causal", [False, True])
