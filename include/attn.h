@@ -25,7 +25,8 @@
  *                         FP32 CUDA-core arithmetic (no tensor cores).
  *  - Supported: d in {64, 128}; N >= 1; B*H*N*d < 2^31; scale finite > 0.
  *  - Ownership: the caller allocates every buffer and owns the stream; the
- *    library allocates no device memory and keeps no per-call state.
+ *    library makes no allocation calls and keeps no per-call state (its one
+ *    fixed device array is described at attn_bwd_noalloc).
  *  - Asynchrony: kernels are enqueued on `stream` and the call returns
  *    without synchronizing.  Argument errors are reported synchronously,
  *    before anything is enqueued; launch failures map to ATTN_ERR_CUDA.
@@ -148,6 +149,32 @@ ATTN_API attn_status attn_check_status(cudaStream_t stream);
  * returns.  attn_check_status() afterwards must report ATTN_ERR_TIMEOUT.
  */
 ATTN_API attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
+
+/*
+ * attn_bwd without a caller workspace, for callers that must not allocate
+ * device memory (no counterpart in the pages: this is a library-usage entry
+ * point, not part of the method).  Typical such callers run inside a host
+ * framework that owns the whole device-memory budget, or in latency-critical
+ * loops where cudaMalloc/cudaFree and their implicit synchronization are not
+ * acceptable.  Same arguments and results as attn_bwd with dt = BF16; the
+ * scratch (LSE*log2(e), delta, FP32 dQ accumulator) lives in a fixed 32 MiB
+ * device array inside the library instead of `workspace`.
+ *   - Limit: attn_bwd_workspace_bytes(B, H, N, d, BF16) must be at most
+ *     33554432 bytes (e.g. B8 H12 N1024 d64 fits); larger problems return
+ *     ATTN_ERR_INVALID_ARG before anything is launched.
+ *   - The array occupies 32 MiB on each GPU where the library's module is
+ *     loaded (at the latest from this entry point's first call there) until
+ *     the process exits.  No call allocates memory.
+ *   - All calls share the array: calls that can overlap on the GPU (other
+ *     streams, unordered host threads) race and give wrong results.  Each call
+ *     rewrites what it reads (the dQ accumulator is zeroed every call).
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture.
+ */
+ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      void* dv, int B, int H, int N, int d, float scale,
+                                      int causal, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

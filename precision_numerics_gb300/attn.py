@@ -23,7 +23,8 @@ ATTN_DTYPE_BF16, ATTN_DTYPE_FP32 = 0, 1
 
 EXPORTED = ("attn_version", "attn_status_string", "attn_last_error", "attn_fwd",
             "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
-            "attn_bwd_dq_convert", "attn_check_status", "attn_selftest_wait_timeout")
+            "attn_bwd_dq_convert", "attn_check_status", "attn_selftest_wait_timeout",
+            "attn_bwd_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -48,6 +49,7 @@ _SIGNATURES = {
     "attn_bwd_dq_convert": (_i, [_vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "attn_check_status": (_i, [_vp]),
     "attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
+    "attn_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
 }
 
 
@@ -214,3 +216,18 @@ def attn_check_status(stream=None) -> None:
 def attn_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     """Enqueue the bounded-wait self-test kernel (see include/attn.h)."""
     _call("attn_selftest_wait_timeout", int(limit_ns), _stream(stream))
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, scale=None, causal=False, stream=None):
+    """attn_bwd for callers that must not allocate device memory: BF16 only,
+    outputs passed in, scratch taken from the library's fixed 32 MiB array
+    (see include/attn.h for the size limit and the sharing rules)."""
+    _check_bhnd("q", q, dtype=torch.bfloat16)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, q.shape, q.dtype)
+    _check_lse(lse, B, H, N)
+    _call("attn_bwd_noalloc", q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+          lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+          _default_scale(d, scale), int(bool(causal)), _stream(stream))
+    return dq, dk, dv

@@ -104,6 +104,8 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
 
 }  // namespace
 
+void set_last_error(const char* msg) { t_last_error = msg; }
+
 EncodeTiledFn encode_tiled_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;

@@ -62,6 +62,9 @@ cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream);
 cudaError_t read_and_clear_status_bwd(unsigned int* out, cudaStream_t stream);
 cudaError_t read_and_clear_status_misc(unsigned int* out, cudaStream_t stream);
 
+// Record the detail text returned by attn_last_error() on this thread.
+void set_last_error(const char* msg);
+
 // Driver entry point for cuTensorMapEncodeTiled (resolved once, no -lcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

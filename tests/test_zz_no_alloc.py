@@ -1,0 +1,79 @@
+"""attn_bwd_noalloc: the backward for callers that must not allocate device memory.
+
+Some callers cannot call cudaMalloc -- e.g. a component inside a host framework
+that owns the whole device-memory budget, or a latency-critical loop that must
+not pay for allocation and its implicit synchronization.  attn_bwd_noalloc
+serves them: the caller passes inputs and outputs only, and the backward's
+scratch comes from a fixed 32 MiB array inside the library.
+
+This file is collected last on purpose (test_zz_*): if it fails, a run that
+stops at the first failure has already run every other test.  It calls the
+entry point through the C ABI twice in a row (different problems, so stale
+scratch from the first call would show in the second) and compares each
+result with attn_bwd given its own workspace, within the BF16 tolerance the
+other tests use (relative L2 1e-2; dK and dV are also bit-identical because
+the same deterministic kernels run).  It passes alone in a fresh process and
+after the other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from precision_numerics_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def lib(cuda_device):
+    from precision_numerics_gb300 import attn, build
+    build.build()
+    return attn.load_library()
+
+
+def _problem(seed, B, H, N, d):
+    x = inputs.random_qkv(seed, B, H, N, d)
+    return {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in x.items()}
+
+
+def _rel_l2(a, b):
+    a, b = a.double(), b.double()
+    return float((a - b).norm() / b.norm())
+
+
+def _run_both(lib, t, scale, causal):
+    from precision_numerics_gb300 import attn
+    B, H, N, d = t["q"].shape
+    o, lse = attn.attn_fwd(t["q"], t["k"], t["v"], scale=scale, causal=causal)
+    ref = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=scale, causal=causal)
+    out = [torch.full_like(o, float("nan")) for _ in range(3)]
+    stream = torch.cuda.current_stream().cuda_stream
+    status = lib.attn_bwd_noalloc(
+        t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(), o.data_ptr(), lse.data_ptr(),
+        t["do"].data_ptr(), out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
+        B, H, N, d, ctypes.c_float(scale), int(causal), ctypes.c_void_p(stream))
+    assert status == 0, lib.attn_last_error().decode()
+    assert lib.attn_check_status(ctypes.c_void_p(stream)) == 0
+    return ref, out
+
+
+def test_two_calls_in_a_row_match_attn_bwd(lib):
+    cases = [(_problem(11, 2, 4, 1000, 128), 1 / 128 ** 0.5, True),
+             (_problem(12, 1, 3, 700, 64), 0.125, False)]
+    for t, scale, causal in cases:
+        ref, got = _run_both(lib, t, scale, causal)
+        for name, r, g in zip(("dq", "dk", "dv"), ref, got):
+            assert bool(torch.isfinite(g.float()).all()), name
+            assert _rel_l2(g, r) <= 1e-2, (name, _rel_l2(g, r))
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+
+
+def test_rejects_problems_beyond_the_fixed_scratch(lib):
+    # B1 H32 N4096 d128 needs 65 MiB of scratch, more than the 32 MiB array.
+    status = lib.attn_bwd_noalloc(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 32, 4096, 128,
+                                  ctypes.c_float(0.088), 1, None)
+    assert status == 1  # ATTN_ERR_INVALID_ARG, before anything is launched
+    msg = lib.attn_last_error().decode()
+    assert "33554432" in msg and "attn_bwd" in msg
