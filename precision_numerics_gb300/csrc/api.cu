@@ -120,12 +120,12 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-bool make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d) {
+bool make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

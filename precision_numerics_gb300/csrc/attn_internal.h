@@ -72,8 +72,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
-// 3-D BF16 tensor map over a [B*H, N, d] tensor with a (64 x 128 x 1) box and
-// 128-byte swizzle.  Returns false when the driver rejects it.
-bool make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d);
+// 3-D BF16 tensor map over a [B*H, N, d] tensor with a (64 x box_rows x 1) box
+// and 128-byte swizzle.  Returns false when the driver rejects it.
+bool make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows = 128);
 
 }  // namespace attn

@@ -30,10 +30,13 @@
 //                   scale * dK (warps 8-11) with TMA stores.
 //   3. dq_convert   dQ = bf16(scale * accumulator).  Memory-bound.
 //
-// TMEM (512 columns): dV [0,d), dK [d,2d), S^T [2d,2d+128), dP^T
-// [2d+128,2d+256).  For d = 128 the dQ tile reuses the S^T columns (the MMA
-// that reads P^T from there is issued first, and tcgen05 MMAs of one thread
-// execute in order); for d = 64 it has its own columns [384,448).
+// Two variants of the main kernel: d = 64 uses 128-row query tiles
+// (bwd_main_kernel below; TMEM dV [0,64), dK [64,128), S^T [128,256), dP^T
+// [256,384), dQ [384,448)); d = 128 uses 64-row query tiles with an
+// overlapped MMA order (r64::bwd_main_d128_kernel, described there).
+// bwd_main_kernel also supports d = 128 (dQ then reuses the S^T columns: the
+// MMA that reads P^T from there is issued first, and tcgen05 MMAs of one
+// thread execute in order).
 #include <math.h>
 
 #include "attn_internal.h"
@@ -526,6 +529,470 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// 2'. main kernel, d = 128: 64-row query tiles, overlapped pipeline
+// ---------------------------------------------------------------------------
+// Same mathematics as bwd_main_kernel, arranged so that the tensor pipe is
+// not left waiting on the P / dS computation or on the dQ drain.  Per
+// 64-row query tile i (index it) the MMAs are
+//   S^T(it)  = K_j Q_i^T     M=128 N=64 K=128   SS  -> S buffer it%2
+//   dP^T(it) = V_j dO_i^T    M=128 N=64 K=128   SS  -> dP region
+//   dV      += P^T dO_i      M=128 N=128 K=64   TS  (P^T in the S buffer)
+//   dK      += dS^T Q_i      M=128 N=128 K=64   TS  (dS^T in the dP region)
+//   dQ^T(it) = K_j^T dS^T    M=128 N=64 K=128   SS  (dS^T from shared memory)
+// issued in the order dV(it), dK(it), dP^T(it+1), dQ^T(it), S^T(it+2), so the
+// P and dS work of tile it+1 runs while the tensor pipe finishes tile it.
+// dQ^T puts head-dim index d on the TMEM lanes: each drain thread owns one d,
+// and a warp's 32 reductions into the FP32 accumulator cover 128 contiguous
+// bytes of one query row.
+// TMEM (512 columns): dV [0,128), dK [128,256), S buffers [256,320) and
+// [320,384), dP [384,448), dQ^T [448,512).  Shared memory: K_j, V_j (32 KB
+// each), a 3-stage ring of Q_i / dO_i (16 KB each) with LSE*log2(e) and delta,
+// and two dS^T buffers (16 KB each).  Each barrier that a role waits on is
+// either completed once per tile or split per buffer, so no waiter can fall
+// two phases behind the barrier it polls.
+namespace r64 {
+
+constexpr int kBM = 64;                    // query rows per tile
+constexpr int kStages = 3;                 // Q / dO ring depth
+constexpr int kKVBytes = 128 * 128 * 2;    // K_j or V_j (128 rows x 128 d)
+constexpr int kKVChunk = 128 * 128;        // one 64-column chunk of K_j / V_j
+constexpr int kQBytes = kBM * 128 * 2;     // Q_i or dO_i (64 rows x 128 d)
+constexpr int kQChunk = kBM * 128;         // one 64-column chunk of Q_i / dO_i
+constexpr int kDSBytes = 128 * kBM * 2;    // dS^T: 128 key rows x 64 query cols
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kKVBytes;
+constexpr int kOffQ = kOffV + kKVBytes;
+constexpr int kOffDO = kOffQ + kStages * kQBytes;
+constexpr int kOffDS = kOffDO + kStages * kQBytes;
+constexpr int kOffLse = kOffDS + 2 * kDSBytes;
+constexpr int kOffDelta = kOffLse + kStages * kBM * 4;
+constexpr int kOffBar = kOffDelta + kStages * kBM * 4;
+// kv_full, q_full[3], q_empty[3], s_full[2], p_ready[2], dp_full, ds_ready,
+// dq_full, dq_free, dq_done[2], dkv_done, mma_final, epi_dv, epi_dk
+constexpr int kNumBars = 1 + 3 + 3 + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 1 + 1 + 1 + 1;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ = 448;
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_d128_kernel(const __grid_constant__ CUtensorMap tmQ,   // box 64 rows
+                         const __grid_constant__ CUtensorMap tmK,   // box 128 rows
+                         const __grid_constant__ CUtensorMap tmV,   // box 128 rows
+                         const __grid_constant__ CUtensorMap tmDO,  // box 64 rows
+                         const __grid_constant__ CUtensorMap tmDK,  // box 128 rows
+                         const __grid_constant__ CUtensorMap tmDV,  // box 128 rows
+                         const float* __restrict__ lse2, const float* __restrict__ delta,
+                         float* __restrict__ dqacc, int BH, int N, int Npad, float scale,
+                         float scale_log2) {
+  constexpr int D = 128;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Key tiles with the most query tiles (causal: small j) first.
+  const int j = blockIdx.x / BH;
+  const int bh = blockIdx.x % BH;
+  const int n_qt = (N + kBM - 1) / kBM;
+  const int i_first = CAUSAL ? 2 * j : 0;
+  const int nq = max(0, n_qt - i_first);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bar_kv = bars + 0;
+  uint64_t* bar_qfull = bars + 1;    // [3]
+  uint64_t* bar_qempty = bars + 4;   // [3]
+  uint64_t* bar_sfull = bars + 7;    // [2]
+  uint64_t* bar_pready = bars + 9;   // [2]
+  uint64_t* bar_dpfull = bars + 11;
+  uint64_t* bar_dsready = bars + 12;
+  uint64_t* bar_dqfull = bars + 13;
+  uint64_t* bar_dqfree = bars + 14;
+  uint64_t* bar_dqdone = bars + 15;  // [2]
+  uint64_t* bar_dkvdone = bars + 17;
+  uint64_t* bar_final = bars + 18;
+  uint64_t* bar_epi_dv = bars + 19;
+  uint64_t* bar_epi_dk = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    *s_abort = (smem_u32(smem) & 1023u) != 0;
+    if (*s_abort) set_fail(ATTN_ERR_INVALID_ARG);
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_qfull[s], 1);
+      mbar_init(&bar_qempty[s], 1 + 4);  // MMA commit + one arrive per compute warp
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_sfull[b], 1);
+      mbar_init(&bar_pready[b], 128);
+      mbar_init(&bar_dqdone[b], 1);
+    }
+    mbar_init(bar_dpfull, 1);
+    mbar_init(bar_dsready, 128);
+    mbar_init(bar_dqfull, 1);
+    mbar_init(bar_dqfree, 128);
+    mbar_init(bar_dkvdone, 1);
+    mbar_init(bar_final, 1);
+    mbar_init(bar_epi_dv, 128);
+    mbar_init(bar_epi_dk, 128);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool abort_all = *s_abort != 0 || nq == 0;
+
+  uint8_t* sK = smem + kOffK;
+  uint8_t* sV = smem + kOffV;
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sDO = smem + kOffDO;
+  uint8_t* sDS = smem + kOffDS;
+  float* sLse = reinterpret_cast<float*>(smem + kOffLse);
+  float* sDelta = reinterpret_cast<float*>(smem + kOffDelta);
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (warp == 0 && lane == 0 && !abort_all) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(bar_kv, 2 * kKVBytes);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(sK + c * kKVChunk, &tmK, bar_kv, c * 64, j * kBlockN, bh);
+        tma_load_3d(sV + c * kKVChunk, &tmV, bar_kv, c * 64, j * kBlockN, bh);
+      }
+      bool ok = true;
+      int issued = 0;
+      for (int it = 0; it < nq; ++it) {
+        const int st = it % kStages, use = it / kStages;
+        const int i = i_first + it;
+        if (use > 0 && !mbar_wait(&bar_qempty[st], (use - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bar_qfull[st], 2 * kQBytes + 2 * kBM * 4);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(sQ + st * kQBytes + c * kQChunk, &tmQ, &bar_qfull[st], c * 64, i * kBM, bh);
+          tma_load_3d(sDO + st * kQBytes + c * kQChunk, &tmDO, &bar_qfull[st], c * 64, i * kBM,
+                      bh);
+        }
+        const size_t prow = (size_t)bh * Npad + (size_t)i * kBM;
+        bulk_load(sLse + st * kBM, lse2 + prow, kBM * 4, &bar_qfull[st]);
+        bulk_load(sDelta + st * kBM, delta + prow, kBM * 4, &bar_qfull[st]);
+        issued = it + 1;
+      }
+      if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      mbar_wait(bar_kv, 0);
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        mbar_wait(&bar_qfull[it % kStages], (it / kStages) & 1);
+    } else if (warp == 1 && lane == 0 && !abort_all) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16(128, kBM, false, false);  // K-major A and B
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // TMEM A, MN-major B
+      constexpr uint32_t idesc_dq = idesc_bf16(128, kBM, true, true);   // MN-major A and B
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ),
+                     aDO = smem_u32(sDO), aDS = smem_u32(sDS);
+      // S^T(it) or dP^T(it) = X_j Y_i^T over the 128 head dims (two 64-column chunks).
+      auto issue_xy = [&](uint32_t d_col, uint32_t aX, uint32_t aY) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t cx = (kk >> 2) * kKVChunk + (kk & 3) * 32;
+          const uint32_t cy = (kk >> 2) * kQChunk + (kk & 3) * 32;
+          mma_ss(tmem + d_col, sdesc_sw128(aX + cx, 16, 1024), sdesc_sw128(aY + cy, 16, 1024),
+                 idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar_kv, 0);
+      // Prologue: S^T(0), dP^T(0), S^T(1).
+      if (ok) ok = mbar_wait(&bar_qfull[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_xy(kColS, aK, aQ);
+        mma_commit(&bar_sfull[0]);
+        issue_xy(kColDP, aV, aDO);
+        mma_commit(bar_dpfull);
+      }
+      if (ok && nq > 1) {
+        ok = mbar_wait(&bar_qfull[1], 0);
+        if (ok) {
+          tc_fence_after();
+          issue_xy(kColS + kBM, aK, aQ + kQBytes);
+          mma_commit(&bar_sfull[1]);
+        }
+      }
+      for (int it = 0; it < nq && ok; ++it) {
+        const int st = it % kStages, b = it & 1;
+        const uint32_t qoff = aQ + st * kQBytes, dooff = aDO + st * kQBytes;
+        // dV += P^T dO_i
+        if (!mbar_wait(&bar_pready[b], (it >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          mma_ts(tmem + kColDV, tmem + kColS + b * kBM + kk * 8,
+                 sdesc_sw128(dooff + kk * 2048, kQChunk, 1024), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i
+        if (!mbar_wait(bar_dsready, it & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          mma_ts(tmem + kColDK, tmem + kColDP + kk * 8,
+                 sdesc_sw128(qoff + kk * 2048, kQChunk, 1024), idesc_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_qempty[st]);
+        // dP^T(it+1): the dP region is free (dK(it) above read dS^T from it).
+        if (it + 1 < nq) {
+          const int st1 = (it + 1) % kStages;
+          issue_xy(kColDP, aV, aDO + st1 * kQBytes);
+          mma_commit(bar_dpfull);
+        }
+        // dQ^T(it) = K_j^T dS^T(it)
+        if (it > 0 && !mbar_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ss(tmem + kColDQ, sdesc_sw128(aK + kk * 2048, kKVChunk, 1024),
+                 sdesc_sw128(aDS + b * kDSBytes + kk * 2048, kDSBytes, 1024), idesc_dq,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(bar_dqfull);
+        mma_commit(&bar_dqdone[b]);
+        // S^T(it+2) into buffer b (P^T(it) was read by dV(it) above).
+        if (it + 2 < nq) {
+          const int st2 = (it + 2) % kStages;
+          if (!mbar_wait(&bar_qfull[st2], ((it + 2) / kStages) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_xy(kColS + b * kBM, aK, aQ + st2 * kQBytes);
+          mma_commit(&bar_sfull[b]);
+        }
+      }
+      if (ok) mma_commit(bar_dkvdone);
+      else set_fail(ATTN_ERR_TIMEOUT);
+      mma_commit(bar_final);
+      mbar_wait(bar_final, 0);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    // -------------------------------------------------- P and dS (key rows)
+    const int r = (warp & 3) * 32 + lane;  // key row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tDP = tmem + lane_off + kColDP;
+    const int kv = j * kBlockN + r;
+    const bool key_valid = kv < N;
+    const uint32_t aDS = smem_u32(sDS);
+    bool ok = !abort_all;
+    for (int it = 0; it < nq && ok; ++it) {
+      const int st = it % kStages, b = it & 1;
+      const int i = i_first + it;
+      const uint32_t tS = tmem + lane_off + kColS + b * kBM;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_qfull[st], (it / kStages) & 1));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_sfull[b], (it >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t p[2][32];
+      tmem_ld32(tS, p[0]);
+      tmem_ld32(tS + 32, p[1]);
+      tmem_wait_ld();
+      reg_fence(p[0]);
+      reg_fence(p[1]);
+      const float* L2 = sLse + st * kBM;
+      // Query columns before vis_from see this key (causal); padded keys see
+      // nothing; padded queries have LSE*log2(e) = +inf, so their P is 0.
+      const int vis_to = CAUSAL ? kv - i * kBM : 0;  // P = 0 for query column c < vis_to
+#pragma unroll
+      for (int c = 0; c < kBM; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cc = c + e;
+          float pv = ex2(fmaf(__uint_as_float(p[cc >> 5][cc & 31]), scale_log2, -lv[e]));
+          if (!key_valid || cc < vis_to) pv = 0.f;
+          p[cc >> 5][cc & 31] = __float_as_uint(pv);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(p[c][2 * e]), __uint_as_float(p[c][2 * e + 1]));
+        tmem_st16(tS + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_pready[b]);
+
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dpfull, it & 1));
+      if (!ok) break;
+      // dS^T buffer b is free once dQ^T(it-2), which read it, has completed.
+      if (it >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_dqdone[b], ((it >> 1) - 1) & 1));
+        if (!ok) break;
+      }
+      tc_fence_after();
+      const float* Dl = sDelta + st * kBM;
+      const uint32_t dsBase = aDS + b * kDSBytes;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dp[32];
+        tmem_ld32(tDP + c * 32, dp);
+        tmem_wait_ld();
+        reg_fence(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = c * 32 + 2 * e;
+          const float2 d2 = *reinterpret_cast<const float2*>(Dl + c0);
+          const float ds0 = __uint_as_float(p[c][2 * e]) * (__uint_as_float(dp[2 * e]) - d2.x);
+          const float ds1 =
+              __uint_as_float(p[c][2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - d2.y);
+          pk[e] = pack_bf16x2(ds0, ds1);
+        }
+        tmem_st16(tDP + c * 16, pk);
+        // dS^T row r, query columns 32c .. 32c+31: 16-byte units 4c .. 4c+3 of
+        // the row's 128-byte swizzled line (query-contiguous, MN-major B of dQ^T).
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(dsBase + sw128_offset(r, c * 4 + u), pk[4 * u], pk[4 * u + 1],
+                       pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_dsready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_qempty[st]);
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+    // ---------------------------------------------------------- dV epilogue
+    if (ok && !abort_all) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dkvdone, 0));
+      if (ok) {
+        tc_fence_after();
+        const uint32_t tDV = tmem + lane_off + kColDV;
+        const uint32_t aStage = smem_u32(sQ);  // the Q ring is free after the loop
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tDV + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+          const uint32_t base = aStage + (c >> 1) * kKVChunk;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(base + sw128_offset(r, (c & 1) * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar_epi_dv);
+        if (r == 0) {
+          if (mbar_wait(bar_epi_dv, 0)) {
+            for (int c = 0; c < 2; ++c)
+              tma_store_3d(&tmDV, sQ + c * kKVChunk, c * 64, j * kBlockN, bh);
+            bulk_commit_group();
+            bulk_wait_group0();
+          } else {
+            set_fail(ATTN_ERR_TIMEOUT);
+          }
+        }
+      } else {
+        set_fail(ATTN_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    // ------------------------------------------------------------ dQ drain
+    const int r = (warp & 3) * 32 + lane;  // head-dim index = TMEM lane of dQ^T
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tDQ = tmem + lane_off + kColDQ;
+    bool ok = !abort_all;
+    for (int it = 0; it < nq && ok; ++it) {
+      const int i = i_first + it;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dqfull, it & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t acc[2][32];
+      tmem_ld32(tDQ, acc[0]);
+      tmem_ld32(tDQ + 32, acc[1]);
+      tmem_wait_ld();
+      reg_fence(acc[0]);
+      reg_fence(acc[1]);
+      tc_fence_before();
+      mbar_arrive(bar_dqfree);
+      // Column c of dQ^T is query row i*64 + c; lane r adds its head dim.
+      float* dst = dqacc + ((size_t)bh * Npad + (size_t)i * kBM) * D + r;
+#pragma unroll
+      for (int c = 0; c < kBM; ++c)
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)c * D),
+                     "f"(__uint_as_float(acc[c >> 5][c & 31]))
+                     : "memory");
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+    // ---------------------------------------------------------- dK epilogue
+    if (ok && !abort_all) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dkvdone, 0));
+      if (ok) {
+        tc_fence_after();
+        const uint32_t tDK = tmem + lane_off + kColDK;
+        const int rk = r;  // key row = TMEM lane of dK
+        const uint32_t aStage = smem_u32(sDO);  // the dO ring is free after the loop
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tDK + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * scale,
+                                __uint_as_float(o[2 * e + 1]) * scale);
+          const uint32_t base = aStage + (c >> 1) * kKVChunk;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(base + sw128_offset(rk, (c & 1) * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar_epi_dk);
+        if (r == 0) {
+          if (mbar_wait(bar_epi_dk, 0)) {
+            for (int c = 0; c < 2; ++c)
+              tma_store_3d(&tmDK, sDO + c * kKVChunk, c * 64, j * kBlockN, bh);
+            bulk_commit_group();
+            bulk_wait_group0();
+          } else {
+            set_fail(ATTN_ERR_TIMEOUT);
+          }
+        }
+      } else {
+        set_fail(ATTN_ERR_TIMEOUT);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace r64
+
 template <int D>
 cudaError_t preprocess_impl(const Problem& p, const void* o, const void* dout, const float* lse,
                             const BwdWorkspace& ws, cudaStream_t stream) {
@@ -566,6 +1033,22 @@ cudaError_t main_impl(const Problem& p, const CUtensorMap* maps, const BwdWorksp
   return cudaGetLastError();
 }
 
+template <bool CAUSAL>
+cudaError_t main_d128_impl(const Problem& p, const CUtensorMap* maps, const BwdWorkspace& ws,
+                           cudaStream_t stream) {
+  auto kernel = r64::bwd_main_d128_kernel<CAUSAL>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         r64::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int BH = p.B * p.H;
+  const int Npad = n_pad(p.N);
+  const int n_kt = Npad / kBlockN;
+  kernel<<<dim3(BH * n_kt), dim3(kThreads), r64::kSmemBytes, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.lse2, ws.delta, ws.dqacc, BH, p.N,
+      Npad, p.scale, p.scale * 1.4426950408889634f);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_preprocess_bf16(const Problem& p, const void* o, const void* dout,
@@ -587,11 +1070,15 @@ cudaError_t launch_bwd_main_bf16(const Problem& p, const void* q, const void* k,
   const int BH = p.B * p.H;
   CUtensorMap maps[6];
   const void* ptrs[6] = {q, k, v, dout, dk, dv};
+  // d = 128 streams 64-row query tiles (Q and dO maps with 64-row boxes).
+  const int q_rows = p.d == 128 ? r64::kBM : kBlockM;
+  const int box_rows[6] = {q_rows, kBlockN, kBlockN, q_rows, kBlockN, kBlockN};
   for (int i = 0; i < 6; ++i)
-    if (!make_tmap_bhnd(&maps[i], ptrs[i], BH, p.N, p.d)) return cudaErrorInvalidValue;
+    if (!make_tmap_bhnd(&maps[i], ptrs[i], BH, p.N, p.d, box_rows[i]))
+      return cudaErrorInvalidValue;
   if (p.d == 128)
-    return p.causal ? main_impl<128, true>(p, maps, ws, stream)
-                    : main_impl<128, false>(p, maps, ws, stream);
+    return p.causal ? main_d128_impl<true>(p, maps, ws, stream)
+                    : main_d128_impl<false>(p, maps, ws, stream);
   return p.causal ? main_impl<64, true>(p, maps, ws, stream)
                   : main_impl<64, false>(p, maps, ws, stream);
 }
