@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sDelta = reinterpret_cast<float*>(smem + C::kOffDelta);
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
     if (warp == 0 && lane == 0 && !abort_all) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&tmQ);
@@ -257,69 +257,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_kv, 0);
       for (int it = max(0, issued - 2); it < issued; ++it)
         mbar_wait(&bar_qfull[it & 1], (it >> 1) & 1);
-    } else if (warp == 1 && lane == 0 && !abort_all) {
+    } else if (warp == 1 && !abort_all) {
       // ------------------------------------------------------------ MMA issuer
+      // Whole warp, warp-uniform operands; elect.sync picks the issuing lane.
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);  // K-major A and B
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // TMEM A, MN-major B
       constexpr uint32_t idesc_dq = idesc_bf16(128, D, true, true);     // MN-major A and B
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ),
-                     aDO = smem_u32(sDO), aDS = smem_u32(sDS);
-      bool ok = mbar_wait(bar_kv, 0);
+      const uint64_t kK = sdesc_sw128(smem_u32(sK), 16, 1024);          // K-major views
+      const uint64_t kV = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t kQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t kDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t mQ = sdesc_sw128(smem_u32(sQ), C::kChunkBytes, 1024);  // MN-major views
+      const uint64_t mDO = sdesc_sw128(smem_u32(sDO), C::kChunkBytes, 1024);
+      const uint64_t mDS = sdesc_sw128(smem_u32(sDS), C::kChunkBytes, 1024);
+      const uint64_t mK = sdesc_sw128(smem_u32(sK), C::kChunkBytes, 1024);
+      bool ok = warp_wait(bar_kv, 0);
       for (int it = 0; it < nq && ok; ++it) {
         const int st = it & 1, use = it >> 1;
-        if (!mbar_wait(&bar_qfull[st], use & 1)) { ok = false; break; }
-        if (C::kDqAliasesS && it > 0 && !mbar_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(&bar_qfull[st], use & 1)) { ok = false; break; }
+        if (C::kDqAliasesS && it > 0 && !warp_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t qoff = aQ + st * C::kTileBytes, dooff = aDO + st * C::kTileBytes;
+        const uint32_t so = st * C::kTileBytes;
         // S^T = K_j Q_i^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(qoff + off, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss_elect(tmem + C::kColS, sdesc_add(kK, off), sdesc_add(kQ, so + off), idesc_s,
+                       kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_sfull);
+        mma_commit_elect(bar_sfull);
         // dP^T = V_j dO_i^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(aV + off, 16, 1024),
-                 sdesc_sw128(dooff + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss_elect(tmem + C::kColDP, sdesc_add(kV, off), sdesc_add(kDO, so + off), idesc_s,
+                       kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_dpfull);
+        mma_commit_elect(bar_dpfull);
         // dV += P^T dO_i
-        if (!mbar_wait(bar_pready, it & 1)) { ok = false; break; }
+        if (!warp_wait(bar_pready, it & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlockM / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
-                 sdesc_sw128(dooff + kk * 2048, C::kChunkBytes, 1024), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_elect(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_add(mDO, so + kk * 2048),
+                       idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q_i
-        if (!mbar_wait(bar_dsready, it & 1)) { ok = false; break; }
+        if (!warp_wait(bar_dsready, it & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlockM / 16; ++kk)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
-                 sdesc_sw128(qoff + kk * 2048, C::kChunkBytes, 1024), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_qempty[st]);
+          mma_ts_elect(tmem + C::kColDK, tmem + C::kColDP + kk * 8, sdesc_add(mQ, so + kk * 2048),
+                       idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(&bar_qempty[st]);
         // dQ_i = dS K_j
-        if (!C::kDqAliasesS && it > 0 && !mbar_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
+        if (!C::kDqAliasesS && it > 0 && !warp_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(aDS + kk * 2048, C::kChunkBytes, 1024),
-                 sdesc_sw128(aK + kk * 2048, C::kChunkBytes, 1024), idesc_dq, kk > 0 ? 1u : 0u);
-        mma_commit(bar_dqfull);
+          mma_ss_elect(tmem + C::kColDQ, sdesc_add(mDS, kk * 2048), sdesc_add(mK, kk * 2048),
+                       idesc_dq, kk > 0 ? 1u : 0u);
+        mma_commit_elect(bar_dqfull);
       }
-      if (ok) mma_commit(bar_dkvdone);
-      else set_fail(ATTN_ERR_TIMEOUT);
-      mma_commit(bar_final);
+      if (ok) mma_commit_elect(bar_dkvdone);
+      else if (lane == 0) set_fail(ATTN_ERR_TIMEOUT);
+      mma_commit_elect(bar_final);
       mbar_wait(bar_final, 0);
     }
     __syncwarp();
   } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // -------------------------------------------------- P and dS (key rows)
     const int r = (warp & 3) * 32 + lane;  // key row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // ------------------------------------------------------------ dQ drain
     const int r = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -658,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sDelta = reinterpret_cast<float*>(smem + kOffDelta);
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
     if (warp == 0 && lane == 0 && !abort_all) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&tmQ);
@@ -692,93 +697,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_kv, 0);
       for (int it = max(0, issued - kStages); it < issued; ++it)
         mbar_wait(&bar_qfull[it % kStages], (it / kStages) & 1);
-    } else if (warp == 1 && lane == 0 && !abort_all) {
+    } else if (warp == 1 && !abort_all) {
       // ------------------------------------------------------------ MMA issuer
+      // Whole warp, warp-uniform operands; elect.sync picks the issuing lane.
       constexpr uint32_t idesc_s = idesc_bf16(128, kBM, false, false);  // K-major A and B
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // TMEM A, MN-major B
       constexpr uint32_t idesc_dq = idesc_bf16(128, kBM, true, true);   // MN-major A and B
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ),
-                     aDO = smem_u32(sDO), aDS = smem_u32(sDS);
-      // S^T(it) or dP^T(it) = X_j Y_i^T over the 128 head dims (two 64-column chunks).
-      auto issue_xy = [&](uint32_t d_col, uint32_t aX, uint32_t aY) {
+      const uint64_t kK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t kV = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t kQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t kDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t mQ = sdesc_sw128(smem_u32(sQ), kQChunk, 1024);
+      const uint64_t mDO = sdesc_sw128(smem_u32(sDO), kQChunk, 1024);
+      const uint64_t mK = sdesc_sw128(smem_u32(sK), kKVChunk, 1024);
+      const uint64_t mDS = sdesc_sw128(smem_u32(sDS), kDSBytes, 1024);
+      // S^T or dP^T (into column d_col) = X_j Y_i^T over the 128 head dims.
+      auto issue_xy = [&](uint32_t d_col, uint64_t dX, uint64_t dY, uint32_t y_off) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t cx = (kk >> 2) * kKVChunk + (kk & 3) * 32;
           const uint32_t cy = (kk >> 2) * kQChunk + (kk & 3) * 32;
-          mma_ss(tmem + d_col, sdesc_sw128(aX + cx, 16, 1024), sdesc_sw128(aY + cy, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss_elect(tmem + d_col, sdesc_add(dX, cx), sdesc_add(dY, y_off + cy), idesc_s,
+                       kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(bar_kv, 0);
+      bool ok = warp_wait(bar_kv, 0);
       // Prologue: S^T(0), dP^T(0), S^T(1).
-      if (ok) ok = mbar_wait(&bar_qfull[0], 0);
+      if (ok) ok = warp_wait(&bar_qfull[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_xy(kColS, aK, aQ);
-        mma_commit(&bar_sfull[0]);
-        issue_xy(kColDP, aV, aDO);
-        mma_commit(bar_dpfull);
+        issue_xy(kColS, kK, kQ, 0);
+        mma_commit_elect(&bar_sfull[0]);
+        issue_xy(kColDP, kV, kDO, 0);
+        mma_commit_elect(bar_dpfull);
       }
       if (ok && nq > 1) {
-        ok = mbar_wait(&bar_qfull[1], 0);
+        ok = warp_wait(&bar_qfull[1], 0);
         if (ok) {
           tc_fence_after();
-          issue_xy(kColS + kBM, aK, aQ + kQBytes);
-          mma_commit(&bar_sfull[1]);
+          issue_xy(kColS + kBM, kK, kQ, kQBytes);
+          mma_commit_elect(&bar_sfull[1]);
         }
       }
       for (int it = 0; it < nq && ok; ++it) {
         const int st = it % kStages, b = it & 1;
-        const uint32_t qoff = aQ + st * kQBytes, dooff = aDO + st * kQBytes;
+        const uint32_t so = st * kQBytes;
         // dV += P^T dO_i
-        if (!mbar_wait(&bar_pready[b], (it >> 1) & 1)) { ok = false; break; }
+        if (!warp_wait(&bar_pready[b], (it >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_ts(tmem + kColDV, tmem + kColS + b * kBM + kk * 8,
-                 sdesc_sw128(dooff + kk * 2048, kQChunk, 1024), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_elect(tmem + kColDV, tmem + kColS + b * kBM + kk * 8,
+                       sdesc_add(mDO, so + kk * 2048), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q_i
-        if (!mbar_wait(bar_dsready, it & 1)) { ok = false; break; }
+        if (!warp_wait(bar_dsready, it & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_ts(tmem + kColDK, tmem + kColDP + kk * 8,
-                 sdesc_sw128(qoff + kk * 2048, kQChunk, 1024), idesc_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_qempty[st]);
+          mma_ts_elect(tmem + kColDK, tmem + kColDP + kk * 8, sdesc_add(mQ, so + kk * 2048),
+                       idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(&bar_qempty[st]);
         // dP^T(it+1): the dP region is free (dK(it) above read dS^T from it).
         if (it + 1 < nq) {
-          const int st1 = (it + 1) % kStages;
-          issue_xy(kColDP, aV, aDO + st1 * kQBytes);
-          mma_commit(bar_dpfull);
+          issue_xy(kColDP, kV, kDO, ((it + 1) % kStages) * kQBytes);
+          mma_commit_elect(bar_dpfull);
         }
         // dQ^T(it) = K_j^T dS^T(it)
-        if (it > 0 && !mbar_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
+        if (it > 0 && !warp_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ss(tmem + kColDQ, sdesc_sw128(aK + kk * 2048, kKVChunk, 1024),
-                 sdesc_sw128(aDS + b * kDSBytes + kk * 2048, kDSBytes, 1024), idesc_dq,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(bar_dqfull);
-        mma_commit(&bar_dqdone[b]);
+          mma_ss_elect(tmem + kColDQ, sdesc_add(mK, kk * 2048),
+                       sdesc_add(mDS, b * kDSBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
+        mma_commit_elect(bar_dqfull);
+        mma_commit_elect(&bar_dqdone[b]);
         // S^T(it+2) into buffer b (P^T(it) was read by dV(it) above).
         if (it + 2 < nq) {
           const int st2 = (it + 2) % kStages;
-          if (!mbar_wait(&bar_qfull[st2], ((it + 2) / kStages) & 1)) { ok = false; break; }
+          if (!warp_wait(&bar_qfull[st2], ((it + 2) / kStages) & 1)) { ok = false; break; }
           tc_fence_after();
-          issue_xy(kColS + b * kBM, aK, aQ + st2 * kQBytes);
-          mma_commit(&bar_sfull[b]);
+          issue_xy(kColS + b * kBM, kK, kQ, st2 * kQBytes);
+          mma_commit_elect(&bar_sfull[b]);
         }
       }
-      if (ok) mma_commit(bar_dkvdone);
-      else set_fail(ATTN_ERR_TIMEOUT);
-      mma_commit(bar_final);
+      if (ok) mma_commit_elect(bar_dkvdone);
+      else if (lane == 0) set_fail(ATTN_ERR_TIMEOUT);
+      mma_commit_elect(bar_final);
       mbar_wait(bar_final, 0);
     }
     __syncwarp();
   } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // -------------------------------------------------- P and dS (key rows)
     const int r = (warp & 3) * 32 + lane;  // key row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -912,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // ------------------------------------------------------------ dQ drain
     const int r = (warp & 3) * 32 + lane;  // head-dim index = TMEM lane of dQ^T
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;

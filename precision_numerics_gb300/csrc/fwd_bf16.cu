@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + C::kOffV;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
     if (warp == 0 && lane == 0 && !abort_all) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&tmQ);
@@ -173,74 +173,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bar_kfull[j % C::kStages], (j / C::kStages) & 1);
       for (int j = max(0, issued_v - C::kStages); j < issued_v; ++j)
         mbar_wait(&bar_vfull[j % C::kStages], (j / C::kStages) & 1);
-    } else if (warp == 1 && lane == 0 && !abort_all) {
+    } else if (warp == 1 && !abort_all) {
       // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs this role with warp-uniform operands; elect.sync
+      // inside each MMA / commit picks the one lane that issues it.
       constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      const int n_t[2] = {n0, n1};
-      bool ok = mbar_wait(bar_q, 0);
+      const uint64_t descQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t descK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t descV = sdesc_sw128(smem_u32(sV), C::kChunkBytes, 1024);
+      bool ok = warp_wait(bar_q, 0);
       auto issue_s = [&](int t, int st) {
+        const uint64_t a0 = sdesc_add(descQ, t * C::kTileBytes);
+        const uint64_t b0 = sdesc_add(descK, st * C::kTileBytes);
+        const uint32_t d = tmem + C::col_s(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(aQ + t * C::kTileBytes + off, 16, 1024);
-          const uint64_t b = sdesc_sw128(aK + st * C::kTileBytes + off, 16, 1024);
-          mma_ss(tmem + C::col_s(t), a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_ss_elect(d, sdesc_add(a0, off), sdesc_add(b0, off), idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int st, bool acc) {
+        const uint64_t b0 = sdesc_add(descV, st * C::kTileBytes);
+        const uint32_t d = tmem + C::col_o(t), a = tmem + C::col_s(t);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(aV + st * C::kTileBytes + kk * 2048, C::kChunkBytes, 1024);
-          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, b, idesc_pv,
-                 (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts_elect(d, a + kk * 8, sdesc_add(b0, kk * 2048), idesc_pv,
+                       (acc || kk > 0) ? 1u : 0u);
       };
       if (ok && nmax > 0) {
-        ok = mbar_wait(&bar_kfull[0], 0);
+        ok = warp_wait(&bar_kfull[0], 0);
         tc_fence_after();
         if (ok) {
-          for (int t = 0; t < 2; ++t)
-            if (n_t[t] > 0) {
-              issue_s(t, 0);
-              mma_commit(&bar_sfull[t]);
-            }
+          if (n0 > 0) {
+            issue_s(0, 0);
+            mma_commit_elect(&bar_sfull[0]);
+          }
+          if (n1 > 0) {
+            issue_s(1, 0);
+            mma_commit_elect(&bar_sfull[1]);
+          }
+          mma_commit_elect(&bar_kempty[0]);  // K_0 is free once S(0) has completed
         }
       }
       for (int j = 0; j < nmax && ok; ++j) {
         const int st = j % C::kStages;
         const int st1 = (j + 1) % C::kStages;
         const bool has_next = j + 1 < nmax;
-        if (!mbar_wait(&bar_vfull[st], (j / C::kStages) & 1)) { ok = false; break; }
-        if (has_next && !mbar_wait(&bar_kfull[st1], ((j + 1) / C::kStages) & 1)) {
+        if (!warp_wait(&bar_vfull[st], (j / C::kStages) & 1)) { ok = false; break; }
+        if (has_next && !warp_wait(&bar_kfull[st1], ((j + 1) / C::kStages) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n_t[t]) continue;
-          if (!mbar_wait(&bar_pfull[t], j & 1)) { ok = false; break; }
+          if (j >= (t == 0 ? n0 : n1)) continue;
+          if (!warp_wait(&bar_pfull[t], j & 1)) { ok = false; break; }
           tc_fence_after();
           issue_pv(t, st, j > 0);
-          if (j + 1 < n_t[t]) {
+          if (j + 1 < (t == 0 ? n0 : n1)) {
             issue_s(t, st1);
-            mma_commit(&bar_sfull[t]);
+            mma_commit_elect(&bar_sfull[t]);
           } else {
-            mma_commit(&bar_odone[t]);
+            mma_commit_elect(&bar_odone[t]);
           }
         }
-        mma_commit(&bar_vempty[st]);
-        mma_commit(&bar_kempty[st]);
+        mma_commit_elect(&bar_vempty[st]);
+        // Release K_{j+1} as soon as the S(j+1) products above have read it, so
+        // the producer can start loading K_{j+1+S} a full iteration ahead.
+        if (has_next) mma_commit_elect(&bar_kempty[st1]);
       }
-      if (!ok) set_fail(ATTN_ERR_TIMEOUT);
-      // Every MMA this thread issued completes before TMEM is released.
-      mma_commit(bar_final);
+      if (!ok && lane == 0) set_fail(ATTN_ERR_TIMEOUT);
+      // Every MMA this warp issued completes before TMEM is released.
+      mma_commit_elect(bar_final);
       mbar_wait(bar_final, 0);
     }
     __syncwarp();
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // -------------------------------------------------------------- softmax
     const int t = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
@@ -270,14 +280,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(s[0][0]);
+      // Row max as four independent chains of three-input maxima (short
+      // dependency chains: only two softmax warps share an SM sub-partition).
+      float mx4[4];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c >> 5][c & 31]));
-      const float m_new = fmaxf(m_run, mx);
+      for (int c = 0; c < 4; ++c) {
+        float m = fmaxf(__uint_as_float(s[c][0]), __uint_as_float(s[c][1]));
+#pragma unroll
+        for (int e = 2; e < 32; e += 2)
+          m = fmax3(m, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+        mx4[c] = m;
+      }
+      const float m_new = fmax3(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3], m_run);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float neg_ms = -m_use * scale_log2;
       const float alpha = ex2((m_run - m_use) * scale_log2);
-      float sum0 = 0.f, sum1 = 0.f;
+      float sums[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sums[u] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -285,13 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2(fmaf(__uint_as_float(s[c][2 * i]), scale_log2, neg_ms));
           const float p1 = ex2(fmaf(__uint_as_float(s[c][2 * i + 1]), scale_log2, neg_ms));
-          sum0 += p0;
-          sum1 += p1;
+          sums[(2 * i) & 7] += p0;
+          sums[(2 * i + 1) & 7] += p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
       }
-      l_run = l_run * alpha + (sum0 + sum1);
+      const float tile_sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) +
+                             ((sums[4] + sums[5]) + (sums[6] + sums[7]));
+      l_run = l_run * alpha + tile_sum;
       // Rescale the partial output when any row max in this warp moved.
       // PV(j-1) has completed: the commit that released S(j) covers it.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
