@@ -549,7 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // P and dS work of tile it+1 runs while the tensor pipe finishes tile it.
 // dQ^T puts head-dim index d on the TMEM lanes: each drain thread owns one d,
 // and a warp's 32 reductions into the FP32 accumulator cover 128 contiguous
-// bytes of one query row.
+// bytes of one query row.  Warps 4-11 form two warpgroups that split every
+// tile's 64 query columns (P, dS and the dQ drain) between them, so each SM
+// sub-partition has two warps to overlap the exp, TMEM and reduction latency.
 // TMEM (512 columns): dV [0,128), dK [128,256), S buffers [256,320) and
 // [320,384), dP [384,448), dQ^T [448,512).  Shared memory: K_j, V_j (32 KB
 // each), a 3-stage ring of Q_i / dO_i (16 KB each) with LSE*log2(e) and delta,
@@ -578,6 +580,11 @@ constexpr int kOffBar = kOffDelta + kStages * kBM * 4;
 constexpr int kNumBars = 1 + 3 + 3 + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 1 + 1 + 1 + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ = 448;
+// P^T and dS^T (BF16 pairs) are written by warpgroup h into the first 16 of
+// its own 32 FP32 columns [32h, 32h+32), so neither warpgroup overwrites
+// values the other has not read yet.  K step kk of the dV / dK products
+// (query columns 16kk .. 16kk+15) is then at packed column:
+__host__ __device__ constexpr uint32_t packed_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
 
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -627,17 +634,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_kv, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_qfull[s], 1);
-      mbar_init(&bar_qempty[s], 1 + 4);  // MMA commit + one arrive per compute warp
+      mbar_init(&bar_qempty[s], 1 + 8);  // MMA commit + one arrive per compute warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_sfull[b], 1);
-      mbar_init(&bar_pready[b], 128);
+      mbar_init(&bar_pready[b], 256);
       mbar_init(&bar_dqdone[b], 1);
     }
     mbar_init(bar_dpfull, 1);
-    mbar_init(bar_dsready, 128);
+    mbar_init(bar_dsready, 256);
     mbar_init(bar_dqfull, 1);
-    mbar_init(bar_dqfree, 128);
+    mbar_init(bar_dqfree, 256);
     mbar_init(bar_dkvdone, 1);
     mbar_init(bar_final, 1);
     mbar_init(bar_epi_dv, 128);
@@ -663,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sDelta = reinterpret_cast<float*>(smem + kOffDelta);
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
     if (warp == 0 && lane == 0 && !abort_all) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&tmQ);
@@ -747,14 +754,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_ts_elect(tmem + kColDV, tmem + kColS + b * kBM + kk * 8,
+          mma_ts_elect(tmem + kColDV, tmem + kColS + b * kBM + packed_col(kk),
                        sdesc_add(mDO, so + kk * 2048), idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q_i
         if (!warp_wait(bar_dsready, it & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_ts_elect(tmem + kColDK, tmem + kColDP + kk * 8, sdesc_add(mQ, so + kk * 2048),
+          mma_ts_elect(tmem + kColDK, tmem + kColDP + packed_col(kk), sdesc_add(mQ, so + kk * 2048),
                        idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit_elect(&bar_qempty[st]);
         // dP^T(it+1): the dP region is free (dK(it) above read dS^T from it).
@@ -785,91 +792,113 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_final, 0);
     }
     __syncwarp();
-  } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
-    // -------------------------------------------------- P and dS (key rows)
-    const int r = (warp & 3) * 32 + lane;  // key row within the tile = TMEM lane
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
+    // ------------------------------- P, dS and the dQ drain (two warpgroups)
+    // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) owns query columns
+    // [32h, 32h+32) of every 64-row tile: it computes those columns of P^T
+    // and dS^T (thread = key row = TMEM lane) and drains those columns of
+    // dQ^T (thread = head dim = TMEM lane).  The drain of dQ^T(it-1) runs at
+    // the end of iteration it, after dS(it); dQ^T(it) needs dS(it), so the
+    // drain is never more than one product behind.
+    const int h = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tDP = tmem + lane_off + kColDP;
+    const uint32_t tDQ = tmem + lane_off + kColDQ + h * 32;
     const int kv = j * kBlockN + r;
     const bool key_valid = kv < N;
-    const uint32_t aDS = smem_u32(sDS);
+    const uint32_t dsBase0 = smem_u32(sDS);
     bool ok = !abort_all;
+    // dQ^T(itd), query columns [32h, 32h+32): lane r adds head dim r of 32 query
+    // rows; a warp's 32 reductions cover 128 contiguous bytes of one row.
+    auto drain = [&](int itd) -> bool {
+      if (!warp_wait(bar_dqfull, itd & 1)) return false;
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tDQ, acc);
+      tmem_wait_ld();
+      reg_fence(acc);
+      tc_fence_before();
+      mbar_arrive(bar_dqfree);
+      float* dst = dqacc + ((size_t)bh * Npad + (size_t)(i_first + itd) * kBM + h * 32) * D + r;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)c * D),
+                     "f"(__uint_as_float(acc[c]))
+                     : "memory");
+      return true;
+    };
     for (int it = 0; it < nq && ok; ++it) {
       const int st = it % kStages, b = it & 1;
       const int i = i_first + it;
       const uint32_t tS = tmem + lane_off + kColS + b * kBM;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_qfull[st], (it / kStages) & 1));
+      ok = warp_wait(&bar_qfull[st], (it / kStages) & 1);
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_sfull[b], (it >> 1) & 1));
+      ok = warp_wait(&bar_sfull[b], (it >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
-      uint32_t p[2][32];
-      tmem_ld32(tS, p[0]);
-      tmem_ld32(tS + 32, p[1]);
+      uint32_t p[32];
+      tmem_ld32(tS + h * 32, p);
       tmem_wait_ld();
-      reg_fence(p[0]);
-      reg_fence(p[1]);
-      const float* L2 = sLse + st * kBM;
-      // Query columns before vis_from see this key (causal); padded keys see
-      // nothing; padded queries have LSE*log2(e) = +inf, so their P is 0.
-      const int vis_to = CAUSAL ? kv - i * kBM : 0;  // P = 0 for query column c < vis_to
+      reg_fence(p);
+      const float* L2 = sLse + st * kBM + h * 32;
+      // Local column c is query i*64 + 32h + c.  Causal: it sees this key only
+      // when c >= vis_to.  Padded keys see nothing; padded queries have
+      // LSE*log2(e) = +inf, so their P is 0 already.
+      const int vis_to = CAUSAL ? kv - i * kBM - h * 32 : 0;
 #pragma unroll
-      for (int c = 0; c < kBM; c += 4) {
+      for (int c = 0; c < 32; c += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int cc = c + e;
-          float pv = ex2(fmaf(__uint_as_float(p[cc >> 5][cc & 31]), scale_log2, -lv[e]));
+          float pv = ex2(fmaf(__uint_as_float(p[cc]), scale_log2, -lv[e]));
           if (!key_valid || cc < vis_to) pv = 0.f;
-          p[cc >> 5][cc & 31] = __float_as_uint(pv);
+          p[cc] = __float_as_uint(pv);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(p[c][2 * e]), __uint_as_float(p[c][2 * e + 1]));
-        tmem_st16(tS + c * 16, pk);
+          pk[e] = pack_bf16x2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1]));
+        tmem_st16(tS + h * 32, pk);  // inside this warpgroup's own S columns
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_pready[b]);
 
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dpfull, it & 1));
+      ok = warp_wait(bar_dpfull, it & 1);
       if (!ok) break;
       // dS^T buffer b is free once dQ^T(it-2), which read it, has completed.
       if (it >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_dqdone[b], ((it >> 1) - 1) & 1));
+        ok = warp_wait(&bar_dqdone[b], ((it >> 1) - 1) & 1);
         if (!ok) break;
       }
       tc_fence_after();
-      const float* Dl = sDelta + st * kBM;
-      const uint32_t dsBase = aDS + b * kDSBytes;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      const float* Dl = sDelta + st * kBM + h * 32;
+      {
         uint32_t dp[32];
-        tmem_ld32(tDP + c * 32, dp);
+        tmem_ld32(tDP + h * 32, dp);
         tmem_wait_ld();
         reg_fence(dp);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int c0 = c * 32 + 2 * e;
-          const float2 d2 = *reinterpret_cast<const float2*>(Dl + c0);
-          const float ds0 = __uint_as_float(p[c][2 * e]) * (__uint_as_float(dp[2 * e]) - d2.x);
-          const float ds1 =
-              __uint_as_float(p[c][2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - d2.y);
+          const float2 d2 = *reinterpret_cast<const float2*>(Dl + 2 * e);
+          const float ds0 = __uint_as_float(p[2 * e]) * (__uint_as_float(dp[2 * e]) - d2.x);
+          const float ds1 = __uint_as_float(p[2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - d2.y);
           pk[e] = pack_bf16x2(ds0, ds1);
         }
-        tmem_st16(tDP + c * 16, pk);
-        // dS^T row r, query columns 32c .. 32c+31: 16-byte units 4c .. 4c+3 of
-        // the row's 128-byte swizzled line (query-contiguous, MN-major B of dQ^T).
+        tmem_st16(tDP + h * 32, pk);  // inside this warpgroup's own dP columns
+        // dS^T row r, query columns 32h .. 32h+31: 16-byte units 4h .. 4h+3 of
+        // the row's 128-byte swizzled line (MN-major B operand of dQ^T).
+        const uint32_t dsBase = dsBase0 + b * kDSBytes;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          st_shared_v4(dsBase + sw128_offset(r, c * 4 + u), pk[4 * u], pk[4 * u + 1],
+          st_shared_v4(dsBase + sw128_offset(r, h * 4 + u), pk[4 * u], pk[4 * u + 1],
                        pk[4 * u + 2], pk[4 * u + 3]);
       }
       tmem_wait_st();
@@ -878,25 +907,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar_dsready);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_qempty[st]);
+      // dQ^T(it-1) is done or nearly so; the MMA warp needs dq_free only after
+      // it has issued dK(it) and dP^T(it+1).
+      if (it > 0) ok = drain(it - 1);
     }
+    if (ok && !abort_all) ok = drain(nq - 1);
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
-    // ---------------------------------------------------------- dV epilogue
+    // ------------------------- epilogue: h = 0 stores dV, h = 1 stores scale*dK
     if (ok && !abort_all) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dkvdone, 0));
+      ok = warp_wait(bar_dkvdone, 0);
       if (ok) {
         tc_fence_after();
-        const uint32_t tDV = tmem + lane_off + kColDV;
-        const uint32_t aStage = smem_u32(sQ);  // the Q ring is free after the loop
+        const uint32_t tAcc = tmem + lane_off + (h == 0 ? kColDV : kColDK);
+        const float mul = h == 0 ? 1.f : scale;
+        uint8_t* stage = h == 0 ? sQ : sDO;  // the Q / dO rings are free after the loop
+        const uint32_t aStage = smem_u32(stage);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(tDV + c * 32, o);
+          tmem_ld32(tAcc + c * 32, o);
           tmem_wait_ld();
           reg_fence(o);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
           const uint32_t base = aStage + (c >> 1) * kKVChunk;
 #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -904,81 +939,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pk[4 * u + 2], pk[4 * u + 3]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar_epi_dv);
+        uint64_t* bar_epi = h == 0 ? bar_epi_dv : bar_epi_dk;
+        mbar_arrive(bar_epi);
         if (r == 0) {
-          if (mbar_wait(bar_epi_dv, 0)) {
+          if (mbar_wait(bar_epi, 0)) {
+            const CUtensorMap* map = h == 0 ? &tmDV : &tmDK;
             for (int c = 0; c < 2; ++c)
-              tma_store_3d(&tmDV, sQ + c * kKVChunk, c * 64, j * kBlockN, bh);
-            bulk_commit_group();
-            bulk_wait_group0();
-          } else {
-            set_fail(ATTN_ERR_TIMEOUT);
-          }
-        }
-      } else {
-        set_fail(ATTN_ERR_TIMEOUT);
-      }
-    }
-  } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
-    // ------------------------------------------------------------ dQ drain
-    const int r = (warp & 3) * 32 + lane;  // head-dim index = TMEM lane of dQ^T
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tDQ = tmem + lane_off + kColDQ;
-    bool ok = !abort_all;
-    for (int it = 0; it < nq && ok; ++it) {
-      const int i = i_first + it;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dqfull, it & 1));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t acc[2][32];
-      tmem_ld32(tDQ, acc[0]);
-      tmem_ld32(tDQ + 32, acc[1]);
-      tmem_wait_ld();
-      reg_fence(acc[0]);
-      reg_fence(acc[1]);
-      tc_fence_before();
-      mbar_arrive(bar_dqfree);
-      // Column c of dQ^T is query row i*64 + c; lane r adds its head dim.
-      float* dst = dqacc + ((size_t)bh * Npad + (size_t)i * kBM) * D + r;
-#pragma unroll
-      for (int c = 0; c < kBM; ++c)
-        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)c * D),
-                     "f"(__uint_as_float(acc[c >> 5][c & 31]))
-                     : "memory");
-    }
-    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
-    // ---------------------------------------------------------- dK epilogue
-    if (ok && !abort_all) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dkvdone, 0));
-      if (ok) {
-        tc_fence_after();
-        const uint32_t tDK = tmem + lane_off + kColDK;
-        const int rk = r;  // key row = TMEM lane of dK
-        const uint32_t aStage = smem_u32(sDO);  // the dO ring is free after the loop
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tDK + c * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * scale,
-                                __uint_as_float(o[2 * e + 1]) * scale);
-          const uint32_t base = aStage + (c >> 1) * kKVChunk;
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_shared_v4(base + sw128_offset(rk, (c & 1) * 4 + u), pk[4 * u], pk[4 * u + 1],
-                         pk[4 * u + 2], pk[4 * u + 3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar_epi_dk);
-        if (r == 0) {
-          if (mbar_wait(bar_epi_dk, 0)) {
-            for (int c = 0; c < 2; ++c)
-              tma_store_3d(&tmDK, sDO + c * kKVChunk, c * 64, j * kBlockN, bh);
+              tma_store_3d(map, stage + c * kKVChunk, c * 64, j * kBlockN, bh);
             bulk_commit_group();
             bulk_wait_group0();
           } else {
@@ -990,7 +957,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
