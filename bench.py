@@ -387,6 +387,14 @@ def _fwd_only_tflops(attn, t, o, lse, w, stream, torch, reps=20):
 # deviation report (GPU vs FP64, next to naive BF16 attention vs FP64)
 # ---------------------------------------------------------------------------
 def run_deviation(args):
+    """Numeric-deviation report, one JSON line per workload (head (0,0)).
+
+    For O, LSE, dQ, dK, dV: the tiled GPU kernel, the tiled GPU kernel with
+    the stabilised normaliser (beta = 2), and the naive BF16 attention, each
+    against the FP64 definition.  Also delta = rowsum(dO o O) formed from the
+    GPU's BF16 O (delta_lp, what the backward uses) against delta from the
+    exact O ("Why Low-Precision Transformer Training Fails", Figure 3).
+    """
     import torch
 
     import oracle
@@ -395,27 +403,36 @@ def run_deviation(args):
 
     build.build()
     cases = [("small", None), ("gpt2", None), ("llama7b", None), ("lowrank", 1.0),
-             ("lowrank", 4.0), ("lowrank", 16.0), ("longseq", None)]
+             ("lowrank", 4.0), ("lowrank", 16.0), ("lowrank_ties", 1.0), ("lowrank_ties", 4.0),
+             ("lowrank_ties", 16.0), ("longseq", None)]
     for name, sigma in cases:
         w = inputs.WORKLOADS[name]
         x = inputs.make_inputs(w, seed=0, sigma=sigma)
         t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in x.items()}
-        o, lse = attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
-        g = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale, causal=w.causal)
-        attn.attn_check_status()
+        runs = {}
+        for tag, fwd in (("tiled_gpu", attn.attn_fwd),
+                         ("tiled_gpu_stable", lambda *a, **kw: attn.attn_fwd_stable(*a, beta=2.0, **kw))):
+            o, lse = fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
+            g = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale, causal=w.causal)
+            attn.attn_check_status()
+            runs[tag] = {"o": o, "lse": lse, "dq": g[0], "dk": g[1], "dv": g[2]}
         head = 0
         f = {k: inputs.bf16_bits_to_f32(v.reshape(w.B * w.H, w.N, w.d)[head]) for k, v in x.items()}
         o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
         g_ref = oracle.backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)
         o_nv, lse_nv = oracle.naive_bf16_forward(f["q"], f["k"], f["v"], w.scale, w.causal)
         g_nv = oracle.naive_bf16_backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)
-        gpu = {"o": o, "lse": lse, "dq": g[0], "dk": g[1], "dv": g[2]}
         ref = {"o": o_ref, "lse": lse_ref, "dq": g_ref[0], "dk": g_ref[1], "dv": g_ref[2]}
         naive = {"o": o_nv, "lse": lse_nv, "dq": g_nv[0], "dk": g_nv[1], "dv": g_nv[2]}
-        rep = {"workload": name, "sigma": sigma, "head": head, "tiled_gpu": {}, "naive_bf16": {}}
+        rep = {"workload": name, "sigma": sigma, "head": head, "naive_bf16": {}}
+        for tag, r in runs.items():
+            rep[tag] = {}
+            for k in ref:
+                gv = r[k].reshape(w.B * w.H, *r[k].shape[2:])[head].float().cpu().numpy()
+                rep[tag][k] = deviation(gv, ref[k])
+            o_lp = r["o"].reshape(w.B * w.H, w.N, w.d)[head].float().cpu().numpy()
+            rep[tag]["delta"] = deviation(oracle.delta(f["do"], o_lp), oracle.delta(f["do"], o_ref))
         for k in ref:
-            gv = gpu[k].reshape(w.B * w.H, *gpu[k].shape[2:])[head].float().cpu().numpy()
-            rep["tiled_gpu"][k] = deviation(gv, ref[k])
             rep["naive_bf16"][k] = deviation(naive[k], ref[k])
         print(json.dumps(rep), flush=True)
     return 0

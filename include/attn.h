@@ -88,6 +88,22 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                               cudaStream_t stream);
 
 /*
+ * Forward pass with the stabilised normaliser of "Why Low-Precision Transformer
+ * Training Fails" (Figure 7 and Algorithm 1): while a row's running maximum
+ * r_m of scale * q.k is attained by two or more keys, the exponentials are
+ * taken relative to m = beta * r_m if r_m > 0 and m = 0 if r_m < 0 (r_m = 0:
+ * m = r_m), so that no unnormalised probability exp(S - m) is exactly 1.
+ * Mathematically O and LSE are those of attn_fwd (LSE is formed with the
+ * normaliser actually used); only the rounding differs.  attn_bwd accepts
+ * its outputs unchanged.  BF16 only; beta must be finite and > 1.  Very large
+ * repeated maxima ((beta - 1) * r_m above ~87) underflow the row's
+ * exponentials in FP32 -- a property of the method, not checked.
+ */
+ATTN_API attn_status attn_fwd_stable(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int B, int H, int N, int d, float scale,
+                                     int causal, float beta, attn_dtype dt, cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (0 on invalid
  * arguments).  Layout (internal): LSE*log2(e) and delta, FP32 [B*H][Npad]
  * each, and the FP32 dQ accumulator [B*H][Npad][d], Npad = N rounded up to

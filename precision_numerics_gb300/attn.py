@@ -24,7 +24,7 @@ ATTN_DTYPE_BF16, ATTN_DTYPE_FP32 = 0, 1
 EXPORTED = ("attn_version", "attn_status_string", "attn_last_error", "attn_fwd",
             "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
             "attn_bwd_dq_convert", "attn_check_status", "attn_selftest_wait_timeout",
-            "attn_bwd_noalloc")
+            "attn_bwd_noalloc", "attn_fwd_stable")
 
 
 class AttnError(RuntimeError):
@@ -50,6 +50,7 @@ _SIGNATURES = {
     "attn_check_status": (_i, [_vp]),
     "attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
     "attn_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "attn_fwd_stable": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _f, _i, _vp]),
 }
 
 
@@ -147,6 +148,24 @@ def attn_fwd(q, k, v, scale=None, causal=False, o=None, lse=None, stream=None):
     _check_lse(lse, B, H, N)
     _call("attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
           B, H, N, d, _default_scale(d, scale), int(bool(causal)), _dtype_code(q), _stream(stream))
+    return o, lse
+
+
+def attn_fwd_stable(q, k, v, scale=None, causal=False, beta=2.0, o=None, lse=None, stream=None):
+    """Forward with the stabilised normaliser (beta * repeated row max).  Returns (o, lse)."""
+    _check_bhnd("q", q, dtype=torch.bfloat16)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _check_bhnd(name, t, q.shape, q.dtype)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_bhnd("o", o, q.shape, q.dtype)
+    _check_lse(lse, B, H, N)
+    _call("attn_fwd_stable", q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+          lse.data_ptr(), B, H, N, d, _default_scale(d, scale), int(bool(causal)), float(beta),
+          ATTN_DTYPE_BF16, _stream(stream))
     return o, lse
 
 

@@ -228,6 +228,26 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   return launched(launch_fwd_bf16(p, q, k, v, o, lse, stream), "attn_fwd (bf16)");
 }
 
+attn_status attn_fwd_stable(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int N, int d, float scale, int causal, float beta,
+                            attn_dtype dt, cudaStream_t stream) {
+  Problem p;
+  ATTN_CHECK(check_problem(B, H, N, d, dt, scale, true, &p));
+  p.causal = causal != 0;
+  if (dt != ATTN_DTYPE_BF16)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_stable is implemented for BF16 only");
+  if (!(isfinite(beta) && beta > 1.f))
+    return fail(ATTN_ERR_INVALID_ARG, "beta must be finite and > 1 (got %g)", (double)beta);
+  ATTN_CHECK(check_ptr(q, "q"));
+  ATTN_CHECK(check_ptr(k, "k"));
+  ATTN_CHECK(check_ptr(v, "v"));
+  ATTN_CHECK(check_ptr(o, "o"));
+  ATTN_CHECK(check_ptr(lse, "lse"));
+  if (encode_tiled_fn() == nullptr)
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  return launched(launch_fwd_bf16(p, q, k, v, o, lse, stream, beta), "attn_fwd_stable");
+}
+
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d, attn_dtype dt) {
   Problem p;
   if (check_problem(B, H, N, d, dt, 1.f, false, &p) != ATTN_OK) return 0;

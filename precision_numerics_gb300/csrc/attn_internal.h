@@ -38,8 +38,9 @@ size_t bwd_workspace_bytes(const Problem& p);
 BwdWorkspace bwd_workspace_carve(void* base, const Problem& p);
 
 // Kernel launchers.  Return cudaSuccess or the launch error.
+// beta > 0 selects the stabilised normaliser (beta * repeated row max).
 cudaError_t launch_fwd_bf16(const Problem& p, const void* q, const void* k, const void* v, void* o,
-                            float* lse, cudaStream_t stream);
+                            float* lse, cudaStream_t stream, float beta = 0.f);
 cudaError_t launch_bwd_preprocess_bf16(const Problem& p, const void* o, const void* dout,
                                        const float* lse, const BwdWorkspace& ws,
                                        cudaStream_t stream);

@@ -67,12 +67,12 @@ __device__ __forceinline__ int kv_tiles_for(int q_first, int N, bool causal) {
   return q_last / kBlockN + 1;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool STABLE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     float* __restrict__ lse, int BH, int N, int num_qt, float scale,
-                    float scale_log2) {
+                    float scale_log2, float beta) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -260,7 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_first = q0 + t * kBlockM;
     const int qi = q_first + r;
     const int n = abort_all ? 0 : (t == 0 ? n0 : n1);
-    float m_run = -INFINITY, l_run = 0.f;
+    // m_run: running row max; m_norm: the normaliser the exponentials of the
+    // previous tiles used (equal to m_run except in the stabilised variant).
+    float m_run = -INFINITY, m_norm = -INFINITY, l_run = 0.f;
+    int n_at_max = 0;  // stabilised variant: elements equal to m_run so far (saturates at 2)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_sfull[t], j & 1));
@@ -291,10 +294,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = fmax3(m, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
         mx4[c] = m;
       }
-      const float m_new = fmax3(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3], m_run);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float m_tile = fmax3(mx4[0], mx4[1], mx4[2]);
+      const float tile_max = fmaxf(m_tile, mx4[3]);
+      const float m_new = fmaxf(tile_max, m_run);
+      float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      if (STABLE) {
+        // "Why Low-Precision Transformer Training Fails", Figure 7 / Algorithm 1:
+        // when the row max r_m is attained more than once, normalise by beta * r_m
+        // (r_m > 0) or by 0 (r_m < 0), so that no exp(S - m) equals exactly 1.
+        // The count of elements equal to the running max is kept across tiles.
+        if (tile_max >= m_run) {
+          int cnt = 0;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) cnt += __uint_as_float(s[c >> 5][c & 31]) == tile_max;
+          n_at_max = min(2, (tile_max > m_run ? 0 : n_at_max) + cnt);
+        }
+        if (n_at_max >= 2) m_use = m_new > 0.f ? beta * m_new : (m_new < 0.f ? 0.f : m_new);
+      }
       const float neg_ms = -m_use * scale_log2;
-      const float alpha = ex2((m_run - m_use) * scale_log2);
+      const float alpha = ex2((m_norm - m_use) * scale_log2);
       float sums[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) sums[u] = 0.f;
@@ -332,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar_pfull[t]);
       m_run = m_new;
+      m_norm = m_use;
     }
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
     if (n > 0 && ok) {
@@ -372,8 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (qi < N) {
-          const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
-          lse[(size_t)bh * N + qi] = m_fin * scale + logf(l_run);
+          lse[(size_t)bh * N + qi] = m_norm * scale + logf(l_run);
         }
       } else {
         set_fail(ATTN_ERR_TIMEOUT);
@@ -389,12 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool STABLE>
 cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mo, float* lse,
+                            const CUtensorMap& mv, const CUtensorMap& mo, float* lse, float beta,
                             cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kernel = fwd_bf16_kernel<D, CAUSAL>;
+  auto kernel = fwd_bf16_kernel<D, CAUSAL, STABLE>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -402,24 +420,34 @@ cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUten
   const int num_qt = ceil_div(p.N, 2 * kBlockM);
   const float scale_log2 = p.scale * 1.4426950408889634f;
   kernel<<<dim3(BH * num_qt), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, mo, lse, BH, p.N,
-                                                                       num_qt, p.scale, scale_log2);
+                                                                       num_qt, p.scale, scale_log2,
+                                                                       beta);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const Problem& p, const void* q, const void* k, const void* v, void* o,
-                            float* lse, cudaStream_t stream) {
+                            float* lse, cudaStream_t stream, float beta) {
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv, mo;
   if (!make_tmap_bhnd(&mq, q, BH, p.N, p.d) || !make_tmap_bhnd(&mk, k, BH, p.N, p.d) ||
       !make_tmap_bhnd(&mv, v, BH, p.N, p.d) || !make_tmap_bhnd(&mo, o, BH, p.N, p.d))
     return cudaErrorInvalidValue;
-  if (p.d == 128)
-    return p.causal ? launch_fwd_impl<128, true>(p, mq, mk, mv, mo, lse, stream)
-                    : launch_fwd_impl<128, false>(p, mq, mk, mv, mo, lse, stream);
-  return p.causal ? launch_fwd_impl<64, true>(p, mq, mk, mv, mo, lse, stream)
-                  : launch_fwd_impl<64, false>(p, mq, mk, mv, mo, lse, stream);
+  const bool st = beta > 0.f;  // beta <= 0: the plain kernel
+#define ATTN_FWD_CASE(DD, CC, SS) \
+  if (p.d == DD && (p.causal != 0) == CC && st == SS) \
+    return launch_fwd_impl<DD, CC, SS>(p, mq, mk, mv, mo, lse, beta, stream);
+  ATTN_FWD_CASE(128, true, false)
+  ATTN_FWD_CASE(128, false, false)
+  ATTN_FWD_CASE(64, true, false)
+  ATTN_FWD_CASE(64, false, false)
+  ATTN_FWD_CASE(128, true, true)
+  ATTN_FWD_CASE(128, false, true)
+  ATTN_FWD_CASE(64, true, true)
+  ATTN_FWD_CASE(64, false, true)
+#undef ATTN_FWD_CASE
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream) {

@@ -19,6 +19,10 @@ Workloads (shapes, value distributions, causal flag, softmax scale):
                V, dO ~ N(0,1); causal, scale 1/sqrt(128)
   longseq      B2 H16 N16384 d128, Q,K,V ~ N(0,1)/sqrt(d), dO ~ N(0,1),
                causal, scale 1/sqrt(128)
+  lowrank_ties the low-rank workload with key rows duplicated in pairs
+               (K[2t+1] = K[2t]), so row maxima are attained exactly twice --
+               the repeated-maximum case of "Why Low-Precision Transformer
+               Training Fails", Figure 7
 
 The low-rank workload is the synthetic stand-in for the "similar low-rank
 representations" of "Why Low-Precision Transformer Training Fails"
@@ -84,6 +88,7 @@ class Workload:
     lowrank_rank: int = 0         # > 0: Q = A U, K = B U with U of this many rows
     sigmas: tuple = field(default_factory=tuple)
     backward: bool = True
+    tied_keys: bool = False       # K[2t+1] = K[2t]
 
     def fwd_flops(self) -> float:
         f = 4.0 * self.B * self.H * self.N * self.N * self.d
@@ -101,6 +106,8 @@ WORKLOADS = {
                         lowrank_rank=4, sigmas=(1.0, 4.0, 16.0)),
     "longseq": Workload("longseq", 2, 16, 16384, 128, True, 1.0 / math.sqrt(128),
                         qkv_std=1.0 / math.sqrt(128)),
+    "lowrank_ties": Workload("lowrank_ties", 4, 16, 2048, 128, True, 1.0 / math.sqrt(128),
+                             lowrank_rank=4, sigmas=(1.0, 4.0, 16.0), tied_keys=True),
 }
 
 
@@ -144,6 +151,9 @@ def make_inputs(w: Workload, seed: int = 0, sigma: float | None = None,
         q = normal(seed, STREAM_Q, shape, w.qkv_std)
         k = normal(seed, STREAM_K, shape, w.qkv_std)
         v = normal(seed, STREAM_V, shape, w.qkv_std)
+    if w.tied_keys:
+        k = k.copy()
+        k[..., 1::2, :] = k[..., 0:w.N - (w.N % 2):2, :]
     do = normal(seed, STREAM_DO, shape)
     out = {"q": q, "k": k, "v": v, "do": do}
     if heads is not None:

@@ -101,3 +101,12 @@ def test_binding_rejects_cpu_tensors():
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         attn.load_library(str(tmp_path / "libattn.so"))
+
+
+def test_stable_forward_argument_checks(lib):
+    def call(beta, dt=0):
+        return lib.attn_fwd_stable(16, 16, 16, 16, 16, 1, 1, 128, 64, ctypes.c_float(0.125), 1,
+                                   ctypes.c_float(beta), dt, None)
+    assert call(1.0) == attn.ATTN_ERR_INVALID_ARG
+    assert call(float("inf")) == attn.ATTN_ERR_INVALID_ARG
+    assert call(2.0, dt=1) == attn.ATTN_ERR_UNSUPPORTED

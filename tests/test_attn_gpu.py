@@ -209,3 +209,40 @@ def test_rejects_host_memory(A):
     r = lib.attn_fwd(host.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), lse.data_ptr(),
                      1, 1, 128, 64, 0.125, 0, 0, None)
     assert r == A.ATTN_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- stabilised forward
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 2, 128, 64), (2, 1, 129, 128), (1, 2, 640, 128),
+                                   (1, 1, 1000, 64)], ids=lambda s: "x".join(map(str, s)))
+def test_stable_forward_matches_definition(A, shape, causal):
+    """The stabilised normaliser changes only rounding: O and LSE are the
+    definition's, and the backward from its LSE is the definition's gradient."""
+    B, H, N, d = shape
+    x = inputs.random_qkv(9, B, H, N, d)
+    scale = 1.0 / math.sqrt(d)
+    t = {k: _dev(v, "bf16") for k, v in x.items()}
+    o, lse = A.attn_fwd_stable(t["q"], t["k"], t["v"], scale=scale, causal=causal, beta=2.0)
+    dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=scale, causal=causal)
+    A.attn_check_status()
+    got = {k: _host(v) for k, v in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+    _assert_bf16(got, _oracle(x, "bf16", scale, causal), tag=shape)
+
+
+@pytest.mark.parametrize("beta", [1.05, 2.0])
+def test_stable_forward_on_exactly_repeated_maxima(A, beta):
+    """Keys duplicated in pairs: every row max is attained twice, so the
+    stabilised path normalises by beta * r_m (or 0) throughout."""
+    w = inputs.Workload("ties", 1, 4, 512, 128, True, 1 / math.sqrt(128), lowrank_rank=4,
+                        sigmas=(4.0,), tied_keys=True)
+    x = inputs.make_inputs(w, seed=3, sigma=4.0)
+    t = {k: _dev(v, "bf16") for k, v in x.items()}
+    o, lse = A.attn_fwd_stable(t["q"], t["k"], t["v"], scale=w.scale, causal=True, beta=beta)
+    o2, lse2 = A.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=True)
+    A.attn_check_status()
+    ref = _oracle(x, "bf16", w.scale, True, backward=False)
+    _assert_bf16({"o": _host(o), "lse": _host(lse)}, ref, backward=False)
+    _assert_bf16({"o": _host(o2), "lse": _host(lse2)}, ref, backward=False)
+    # The normaliser differs, so the two kernels round differently somewhere.
+    assert not torch.equal(o, o2)

@@ -62,3 +62,11 @@ def test_workload_flop_counts():
     assert w.fwd_flops() == pytest.approx(137.4e9, rel=1e-3)
     assert w.bwd_flops() == pytest.approx(343.6e9, rel=1e-3)
     assert inputs.WORKLOADS["gpt2"].fwd_flops() == pytest.approx(12.88e9, rel=1e-3)
+
+
+def test_tied_keys_are_exact_pairs():
+    w = inputs.Workload("t", 1, 2, 64, 128, True, 0.1, lowrank_rank=4, sigmas=(4.0,),
+                        tied_keys=True)
+    k = inputs.make_inputs(w, seed=1, sigma=4.0)["k"]
+    np.testing.assert_array_equal(k[..., 1::2, :], k[..., 0::2, :])
+    assert not np.array_equal(k[..., 0, :], k[..., 2, :])
