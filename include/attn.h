@@ -95,9 +95,11 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  * m = r_m), so that no unnormalised probability exp(S - m) is exactly 1.
  * Mathematically O and LSE are those of attn_fwd (LSE is formed with the
  * normaliser actually used); only the rounding differs.  attn_bwd accepts
- * its outputs unchanged.  BF16 only; beta must be finite and > 1.  Very large
- * repeated maxima ((beta - 1) * r_m above ~87) underflow the row's
- * exponentials in FP32 -- a property of the method, not checked.
+ * its outputs unchanged.  BF16 only; beta must be finite and > 1.  The shift
+ * is capped so that the row's largest exponent stays at or above 2^-64: for
+ * very large repeated maxima ((beta - 1) * scale * r_m * log2(e) > 64) the
+ * normaliser is r_m + 64 / (scale * log2(e)) instead of beta * r_m, which
+ * keeps every exponential below 1 without underflowing the whole row.
  */
 ATTN_API attn_status attn_fwd_stable(const void* q, const void* k, const void* v, void* o,
                                      float* lse, int B, int H, int N, int d, float scale,

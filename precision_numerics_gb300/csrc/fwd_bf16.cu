@@ -309,7 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c) cnt += __uint_as_float(s[c >> 5][c & 31]) == tile_max;
           n_at_max = min(2, (tile_max > m_run ? 0 : n_at_max) + cnt);
         }
-        if (n_at_max >= 2) m_use = m_new > 0.f ? beta * m_new : (m_new < 0.f ? 0.f : m_new);
+        if (n_at_max >= 2) {
+          m_use = m_new > 0.f ? beta * m_new : (m_new < 0.f ? 0.f : m_new);
+          // Keep the row's largest exponent c * (r_m - m) at or above -64 (base 2),
+          // so a very large repeated maximum cannot underflow every exponential
+          // of the row (the pages do not discuss that range).
+          m_use = fminf(m_use, m_new + 64.f / scale_log2);
+        }
       }
       const float neg_ms = -m_use * scale_log2;
       const float alpha = ex2((m_norm - m_use) * scale_log2);

@@ -246,3 +246,17 @@ def test_stable_forward_on_exactly_repeated_maxima(A, beta):
     _assert_bf16({"o": _host(o2), "lse": _host(lse2)}, ref, backward=False)
     # The normaliser differs, so the two kernels round differently somewhere.
     assert not torch.equal(o, o2)
+
+
+def test_stable_forward_caps_the_shift_for_huge_repeated_maxima(A):
+    """Low-rank ties at sigma = 16: (beta - 1) * r_m far beyond the FP32 range;
+    the capped normaliser keeps every row finite and exact to tolerance."""
+    w = inputs.Workload("ties16", 1, 2, 512, 128, True, 1 / math.sqrt(128), lowrank_rank=4,
+                        sigmas=(16.0,), tied_keys=True)
+    x = inputs.make_inputs(w, seed=4, sigma=16.0)
+    t = {k: _dev(v, "bf16") for k, v in x.items()}
+    o, lse = A.attn_fwd_stable(t["q"], t["k"], t["v"], scale=w.scale, causal=True, beta=2.0)
+    A.attn_check_status()
+    assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())
+    _assert_bf16({"o": _host(o), "lse": _host(lse)}, _oracle(x, "bf16", w.scale, True, False),
+                 backward=False)
