@@ -14,7 +14,7 @@ Rank 0 prints ONE JSON line.  `value` is whole-job TFLOP/s with inputs
 resident in HBM; `e2e` is the same metric measured through the Python API
 with pinned host buffers (host->device copies of Q, K, V, dO and
 device->host copies of O, LSE, dQ, dK, dV inside the timed region);
-`roofline` describes the dominant kernel (the backward main kernel) timed
+(HostAttention pipelines head groups over three streams); `roofline` describes the dominant kernel (the backward main kernel) timed
 with CUDA events on its stream; `cpu_baseline` is the FP64 oracle timed on
 the host cores on a bounded sample.  `--impl reference` times that oracle
 as the reference arm instead.  Under torchrun every rank runs its own full
@@ -282,20 +282,13 @@ def run_ours(args, w):
     main_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
     attn.attn_check_status()
 
-    # End-to-end through the public API with pinned host buffers.
-    out_host = {k: torch.empty_like(host["q"]).pin_memory() for k in ("o", "dq", "dk", "dv")}
-    out_host["lse"] = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-
-    def e2e_step():
-        t2 = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
-        o_, lse_ = attn.attn_fwd(t2["q"], t2["k"], t2["v"], scale=w.scale, causal=w.causal)
-        dq_, dk_, dv_ = attn.attn_bwd(t2["q"], t2["k"], t2["v"], o_, lse_, t2["do"], scale=w.scale,
-                                      causal=w.causal, workspace=ws)
-        for k_, v_ in (("o", o_), ("lse", lse_), ("dq", dq_), ("dk", dk_), ("dv", dv_)):
-            out_host[k_].copy_(v_, non_blocking=True)
-
-    for _ in range(max(1, min(args.warmup, 3))):
-        e2e_step()
+    # End-to-end through the public API with pinned host buffers: the head
+    # groups are pipelined (H2D copy, kernels, D2H copy on three streams).
+    from precision_numerics_gb300.host import HostAttention
+    pipe = HostAttention(B, H, N, d, scale=w.scale, causal=w.causal, chunks=args.e2e_chunks,
+                         device=dev)
+    for _ in range(max(3, min(args.warmup, 5))):
+        pipe.run(host["q"], host["k"], host["v"], host["do"])
     e2e_steps = max(1, min(args.steps, 20))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -303,11 +296,12 @@ def run_ours(args, w):
         dist.barrier()
     e0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        pipe.run(host["q"], host["k"], host["v"], host["do"])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     attn.attn_check_status()
+    h2d_bytes, d2h_bytes = pipe.bytes_per_run()
     sampler.stop()
 
     # Max over ranks.
@@ -322,8 +316,7 @@ def run_ours(args, w):
         ms_per_step = elapsed_ms / args.steps
         value = world * step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12
         achieved = w.bwd_flops() / (main_ms * 1e-3) / 1e12
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+        h2d, d2h = h2d_bytes, d2h_bytes
 
         # Max error vs FP64 on a sampled head (head 0) of the timed outputs.
         import oracle
@@ -448,6 +441,8 @@ def main():
     ap.add_argument("--deviation", action="store_true",
                     help="print the numeric-deviation report instead of the bench line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="head groups pipelined in the end-to-end (host buffer) measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1,0 +1,99 @@
+"""Attention forward + backward on pinned HOST tensors, pipelined over heads.
+
+Every (b, h) head is independent, so the B*H heads are split into `chunks`
+contiguous groups and, for each group, three streams run in a pipeline:
+the host->device copy of Q, K, V, dO, then attn_fwd and attn_bwd on the
+device, then the device->host copy of O, LSE, dQ, dK, dV.  The copies of one
+group overlap the kernels of its neighbours, and the two copy directions
+overlap each other.  All arithmetic runs in the library's kernels; this
+module only schedules copies and calls.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import attn
+
+
+class HostAttention:
+    """Reusable pipeline for one problem shape (device buffers are reused).
+
+    q, k, v, do: pinned host BF16 tensors [B, H, N, d].  Outputs are written
+    into pinned host tensors allocated once (attributes o, lse, dq, dk, dv);
+    they are complete once the calling stream has passed run()'s end (e.g.
+    after torch.cuda.synchronize()), and the next run() overwrites them.
+    """
+
+    def __init__(self, B, H, N, d, scale=None, causal=False, chunks=4, device=None):
+        self.B, self.H, self.N, self.d = B, H, N, d
+        self.scale, self.causal = scale, causal
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        bh = B * H
+        chunks = max(1, min(chunks, bh))
+        bounds = [round(i * bh / chunks) for i in range(chunks + 1)]
+        self.groups = [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        self.streams = [torch.cuda.Stream(self.device) for _ in range(3)]
+        dt = torch.bfloat16
+        self.o = torch.empty((B, H, N, d), dtype=dt).pin_memory()
+        self.dq = torch.empty((B, H, N, d), dtype=dt).pin_memory()
+        self.dk = torch.empty((B, H, N, d), dtype=dt).pin_memory()
+        self.dv = torch.empty((B, H, N, d), dtype=dt).pin_memory()
+        self.lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        # Device buffers, one set per group, so group g+1's inputs can land while
+        # group g is still being computed or copied out.
+        self.buf = []
+        for a, b in self.groups:
+            n = b - a
+            t = {k: torch.empty((1, n, N, d), dtype=dt, device=self.device)
+                 for k in ("q", "k", "v", "do", "o", "dq", "dk", "dv")}
+            t["lse"] = torch.empty((1, n, N), dtype=torch.float32, device=self.device)
+            t["ws"] = torch.empty(attn.attn_bwd_workspace_bytes(1, n, N, d), dtype=torch.uint8,
+                                  device=self.device)
+            self.buf.append(t)
+        self._last_out = [None] * len(self.groups)  # D2H completion of the previous run
+
+    @staticmethod
+    def _heads(x, a, b):
+        return x.reshape(-1, *x.shape[2:])[a:b].unsqueeze(0)
+
+    def run(self, q, k, v, do):
+        """Enqueue the whole pipeline; the current stream waits for its end."""
+        s_in, s_cmp, s_out = self.streams
+        cur = torch.cuda.current_stream(self.device)
+        s_in.wait_stream(cur)
+        done = []
+        for g, ((a, b), t) in enumerate(zip(self.groups, self.buf)):
+            # This group's device buffers are free once the previous run copied them out.
+            if self._last_out[g] is not None:
+                s_in.wait_event(self._last_out[g])
+            with torch.cuda.stream(s_in):
+                for name, src in (("q", q), ("k", k), ("v", v), ("do", do)):
+                    t[name].copy_(self._heads(src, a, b), non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            s_cmp.wait_event(ev_in)
+            with torch.cuda.stream(s_cmp):
+                attn.attn_fwd(t["q"], t["k"], t["v"], scale=self.scale, causal=self.causal,
+                              o=t["o"], lse=t["lse"], stream=s_cmp)
+                attn.attn_bwd(t["q"], t["k"], t["v"], t["o"], t["lse"], t["do"], scale=self.scale,
+                              causal=self.causal, dq=t["dq"], dk=t["dk"], dv=t["dv"],
+                              workspace=t["ws"], stream=s_cmp)
+                ev_cmp = torch.cuda.Event()
+                ev_cmp.record(s_cmp)
+            s_out.wait_event(ev_cmp)
+            with torch.cuda.stream(s_out):
+                for name, dst in (("o", self.o), ("dq", self.dq), ("dk", self.dk), ("dv", self.dv)):
+                    self._heads(dst, a, b).copy_(t[name], non_blocking=True)
+                self.lse.reshape(-1, self.N)[a:b].copy_(t["lse"][0], non_blocking=True)
+                ev_out = torch.cuda.Event()
+                ev_out.record(s_out)
+            done.append(ev_out)
+            self._last_out[g] = ev_out
+        for ev in done:
+            cur.wait_event(ev)
+        return self.o, self.lse, self.dq, self.dk, self.dv
+
+    def bytes_per_run(self):
+        """Host->device and device->host bytes moved by one run()."""
+        el = self.B * self.H * self.N * self.d * 2
+        return 4 * el, 4 * el + self.B * self.H * self.N * 4

@@ -260,3 +260,25 @@ def test_stable_forward_caps_the_shift_for_huge_repeated_maxima(A):
     assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())
     _assert_bf16({"o": _host(o), "lse": _host(lse)}, _oracle(x, "bf16", w.scale, True, False),
                  backward=False)
+
+
+@pytest.mark.parametrize("chunks", [1, 3])
+def test_host_pipeline_matches_device_path(A, chunks):
+    """HostAttention (pinned host buffers, head groups pipelined over three
+    streams) gives the device path's results; run twice to exercise reuse."""
+    from precision_numerics_gb300.host import HostAttention
+    B, H, N, d = 1, 5, 300, 128
+    x = inputs.random_qkv(10, B, H, N, d)
+    host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in x.items()}
+    t = {k: v.cuda() for k, v in host.items()}
+    o, lse = A.attn_fwd(t["q"], t["k"], t["v"], causal=True)
+    dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=True)
+    pipe = HostAttention(B, H, N, d, causal=True, chunks=chunks)
+    for _ in range(2):
+        ho, hl, hdq, hdk, hdv = pipe.run(host["q"], host["k"], host["v"], host["do"])
+        torch.cuda.synchronize()
+        A.attn_check_status()
+        assert torch.equal(ho, o.cpu()) and torch.equal(hl, lse.cpu())
+        assert torch.equal(hdk, dk.cpu()) and torch.equal(hdv, dv.cpu())
+        rel = float((hdq.float() - dq.float().cpu()).norm() / dq.float().cpu().norm())
+        assert rel <= 1e-2
