@@ -59,6 +59,23 @@ def _peaks():
         return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
 
 
+def _max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks (identity without a group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def _job_tflops(world, flops_per_step, steps, elapsed_ms):
+    """Whole-job throughput: every rank ran `steps` steps of its own workload
+    (weak scaling), timed by the slowest rank."""
+    return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -304,17 +321,13 @@ def run_ours(args, w):
     h2d_bytes, d2h_bytes = pipe.bytes_per_run()
     sampler.stop()
 
-    # Max over ranks.
-    if world > 1:
-        tt = torch.tensor([elapsed_ms, main_ms, e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms, main_ms, e2e_ms = (float(v) for v in tt.tolist())
+    elapsed_ms, main_ms, e2e_ms = _max_over_ranks([elapsed_ms, main_ms, e2e_ms], dev)
 
     if rank == 0:
         peaks = _peaks()
         step_flops = w.fwd_flops() + w.bwd_flops()
         ms_per_step = elapsed_ms / args.steps
-        value = world * step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+        value = _job_tflops(world, step_flops, args.steps, elapsed_ms)
         achieved = w.bwd_flops() / (main_ms * 1e-3) / 1e12
         h2d, d2h = h2d_bytes, d2h_bytes
 
@@ -348,7 +361,7 @@ def run_ours(args, w):
                          "peak_source": f"{peaks['source']} bf16 burst",
                          "traffic": _traffic_per_launch(w.name),
                          "algorithmic": "2.5 * 4*B*H*N^2*d/2 FLOP per launch (5 matmuls)"},
-            "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "e2e": {"value": _job_tflops(world, step_flops, 1, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": sampler.summary(),
