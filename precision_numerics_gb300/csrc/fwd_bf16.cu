@@ -12,13 +12,16 @@
 // even) only as the operand of the P V product; the row sum accumulates the
 // FP32 values.
 //
-// CTA = 2 query tiles of 128 rows (256 rows of one (b, h)), 12 warps:
+// CTA = 2 query tiles of 128 rows (256 rows of one (b, h)), 16 warps:
 //   warp 0      TMA producer (Q once; K_j, V_j through a shared-memory ring)
 //   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
 //   warp 2      TMEM allocation owner
 //   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1; each
 //               thread owns one query row (one TMEM lane), so row max and
 //               row sum need no cross-thread reduction.
+//   warps 12-15 correction: rescale O_t by exp(m_old - m_new) for both tiles
+//               while the softmax warps compute the exponentials, so the
+//               rescale is off the softmax's critical path.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
 // O_1 [256+d,256+2d).  P_t (BF16, two per 32-bit column) overwrites the
 // first 64 columns of S_t and is the A operand of the P V MMA.  The MMA
@@ -35,7 +38,11 @@ static __device__ unsigned int g_status_fwd;
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+// Correction warps: 32-column O chunks loaded per TMEM round trip, and the
+// register split (setmaxnreg) that goes with it.
+constexpr int kCorrChunks = 2;
+constexpr int kRegsCorr = 96, kRegsSoftmax = 168;  // 72 + 96 + 2 * 168 <= 512
 
 template <int D>
 struct FwdCfg {
@@ -48,9 +55,10 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-  // o_done[2], epi[2], mma_final
-  static constexpr int kNumBars = 1 + 4 * kStages + 9;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
+  // o_done[2], epi[2], mma_final, alpha[2][4] (one per tile and softmax warp)
+  static constexpr int kNumBars = 1 + 4 * kStages + 17;
+  static constexpr int kOffAlpha = kOffBar + kNumBars * 8 + 16;  // FP32 [2][128]
+  static constexpr int kSmemBytes = kOffAlpha + 2 * 128 * 4;
   static constexpr uint32_t kTmemCols = 512;
   // TMEM column of S_t and O_t.
   static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
@@ -74,6 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* __restrict__ lse, int BH, int N, int num_qt, float scale,
                     float scale_log2, float beta) {
   using C = FwdCfg<D>;
+  static_assert(72 + kRegsCorr + 2 * kRegsSoftmax <= 512, "setmaxnreg split exceeds the launch pool");
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5;
@@ -96,7 +105,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_odone = bar_pfull + 2;
   uint64_t* bar_epi = bar_odone + 2;
   uint64_t* bar_final = bar_epi + 2;
+  uint64_t* bar_alpha = bar_final + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  float* s_alpha = reinterpret_cast<float*>(smem + C::kOffAlpha);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int n0 = kv_tiles_for(q0, N, CAUSAL);
@@ -115,7 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_sfull[t], 1);
-      mbar_init(&bar_pfull[t], 128);
+      mbar_init(&bar_pfull[t], 256);  // softmax (P stored) + correction (O rescaled)
+      for (int q = 0; q < 4; ++q) mbar_init(&bar_alpha[t * 4 + q], 32);
       mbar_init(&bar_odone[t], 1);
       mbar_init(&bar_epi[t], 128);
     }
@@ -249,8 +261,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_final, 0);
     }
     __syncwarp();
+  } else if (warp >= 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCorr));
+    // -------------------------------------------------------------- correction
+    // O_t(j-1) has completed when the softmax of tile t publishes alpha(j):
+    // that happens after S_t(j) completed, and the commit that signalled S_t(j)
+    // covers every earlier MMA, PV_t(j-1) included.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = !abort_all;
+    for (int j = 0; j < nmax && ok; ++j) {
+      for (int t = 0; t < 2; ++t) {
+        if (j >= (t == 0 ? n0 : n1)) continue;
+        // Only the softmax warp that owns the same 32 TMEM lanes is waited for.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_alpha[t * 4 + (warp & 3)], j & 1));
+        if (!ok) break;
+        const float alpha = s_alpha[t * 128 + r];
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          tc_fence_after();
+          const uint32_t tO = tmem + lane_off + C::col_o(t);
+          const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+          for (int c = 0; c < D / 32; c += kCorrChunks) {  // 32-column chunks per TMEM round trip
+            uint32_t o[kCorrChunks][32];
+#pragma unroll
+            for (int h = 0; h < kCorrChunks; ++h) tmem_ld32(tO + (c + h) * 32, o[h]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < kCorrChunks; ++h) {
+              reg_fence(o[h]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float lo, hi;
+                f2_unpack(mul2(f2_pack(__uint_as_float(o[h][2 * i]), __uint_as_float(o[h][2 * i + 1])),
+                               a2),
+                          lo, hi);
+                o[h][2 * i] = __float_as_uint(lo);
+                o[h][2 * i + 1] = __float_as_uint(hi);
+              }
+              tmem_st32(tO + (c + h) * 32, o[h]);
+            }
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_pfull[t]);
+      }
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // -------------------------------------------------------------- softmax
     const int t = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
@@ -319,39 +379,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float neg_ms = -m_use * scale_log2;
       const float alpha = ex2((m_norm - m_use) * scale_log2);
-      float sums[8];
+      s_alpha[t * 128 + r] = alpha;
+      mbar_arrive(&bar_alpha[t * 4 + (warp & 3)]);  // the correction warp rescales O_t meanwhile
+      // Eight partial row sums held as four packed pairs: element e of the
+      // row goes to partial sum e mod 8.  Packed FP32 pair instructions halve
+      // the FMA-pipe instruction count of the argument and sum updates.
+      uint64_t sums2[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sums[u] = 0.f;
+      for (int u = 0; u < 4; ++u) sums2[u] = 0ull;
+      const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+      const uint64_t nm2 = f2_pack(neg_ms, neg_ms);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[c][2 * i]), scale_log2, neg_ms));
-          const float p1 = ex2(fmaf(__uint_as_float(s[c][2 * i + 1]), scale_log2, neg_ms));
-          sums[(2 * i) & 7] += p0;
-          sums[(2 * i + 1) & 7] += p1;
+          float x0, x1;
+          f2_unpack(fma2(f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
+                         c2, nm2),
+                    x0, x1);
+          const float p0 = ex2(x0);
+          const float p1 = ex2(x1);
+          sums2[i & 3] = add2(sums2[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
       }
+      float sums[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f2_unpack(sums2[u], sums[2 * u], sums[2 * u + 1]);
       const float tile_sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) +
                              ((sums[4] + sums[5]) + (sums[6] + sums[7]));
       l_run = l_run * alpha + tile_sum;
-      // Rescale the partial output when any row max in this warp moved.
-      // PV(j-1) has completed: the commit that released S(j) covers it.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c * 32, o);
-        }
-      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_pfull[t]);
@@ -374,10 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           reg_fence(o);
           uint32_t pk[16];
+          const uint64_t il2 = f2_pack(inv_l, inv_l);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                __uint_as_float(o[2 * i + 1]) * inv_l);
+          for (int i = 0; i < 16; ++i) {
+            float lo, hi;
+            f2_unpack(mul2(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
+                      lo, hi);
+            pk[i] = pack_bf16x2(lo, hi);
+          }
           const uint32_t base = aStage + (c >> 1) * C::kChunkBytes;
 #pragma unroll
           for (int u = 0; u < 4; ++u)
