@@ -107,7 +107,7 @@ ATTN_API attn_status attn_fwd_stable(const void* q, const void* k, const void* v
 
 /*
  * Bytes of device workspace attn_bwd needs for this problem (0 on invalid
- * arguments).  Layout (internal): LSE*log2(e) and delta, FP32 [B*H][Npad]
+ * arguments).  Layout (internal): -LSE*log2(e) and delta, FP32 [B*H][Npad]
  * each, and the FP32 dQ accumulator [B*H][Npad][d], Npad = N rounded up to
  * 128.  The workspace needs no initialisation; attn_bwd overwrites it.
  */
@@ -124,7 +124,7 @@ ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d, attn_dtype 
  *   workspace        : device buffer of at least
  *                      attn_bwd_workspace_bytes(...) bytes, 256-byte aligned,
  *                      not shared with a concurrently running call.
- * Enqueues three kernels on `stream`: preprocess (delta, LSE*log2(e), zero
+ * Enqueues three kernels on `stream`: preprocess (delta, -LSE*log2(e), zero
  * the dQ accumulator), the main kernel (dK, dV, dQ accumulation), and the
  * dQ conversion (scale and round).  The three phases are also exported
  * below so that each can be timed on its own.
@@ -135,7 +135,7 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Phase 1 of attn_bwd (BF16 only): delta_i = rowsum(dO o O)_i in FP32 from
- * the stored O, LSE*log2(e), and a zeroed dQ accumulator, into `workspace`. */
+ * the stored O, -LSE*log2(e), and a zeroed dQ accumulator, into `workspace`. */
 ATTN_API attn_status attn_bwd_preprocess(const void* o, const float* lse, const void* dout, int B,
                                          int H, int N, int d, attn_dtype dt, void* workspace,
                                          size_t workspace_bytes, cudaStream_t stream);
@@ -175,7 +175,7 @@ ATTN_API attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, cud
  * framework that owns the whole device-memory budget, or in latency-critical
  * loops where cudaMalloc/cudaFree and their implicit synchronization are not
  * acceptable.  Same arguments and results as attn_bwd with dt = BF16; the
- * scratch (LSE*log2(e), delta, FP32 dQ accumulator) lives in a fixed 32 MiB
+ * scratch (-LSE*log2(e), delta, FP32 dQ accumulator) lives in a fixed 32 MiB
  * device array inside the library instead of `workspace`.
  *   - Limit: attn_bwd_workspace_bytes(B, H, N, d, BF16) must be at most
  *     33554432 bytes (e.g. B8 H12 N1024 d64 fits); larger problems return

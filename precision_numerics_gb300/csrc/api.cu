@@ -142,7 +142,7 @@ BwdWorkspace bwd_workspace_carve(void* base, const Problem& p) {
   const size_t rows = (size_t)p.B * p.H * n_pad(p.N);
   char* b = static_cast<char*>(base);
   BwdWorkspace ws;
-  ws.lse2 = reinterpret_cast<float*>(b);
+  ws.neg_lse2 = reinterpret_cast<float*>(b);
   ws.delta = reinterpret_cast<float*>(b + align256(rows * 4));
   ws.dqacc = reinterpret_cast<float*>(b + 2 * align256(rows * 4));
   return ws;

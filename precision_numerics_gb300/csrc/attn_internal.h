@@ -26,11 +26,11 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline int n_pad(int N) { return ceil_div(N, kBlockN) * kBlockN; }
 
 // Backward workspace layout (all offsets 256-byte aligned):
-//   lse2  FP32 [B*H][Npad]    LSE * log2(e); +inf for padded rows
+//   neg_lse2 FP32 [B*H][Npad] -(LSE * log2(e)); -inf for padded rows
 //   delta FP32 [B*H][Npad]    rowsum(dO o O); 0 for padded rows
 //   dqacc FP32 [B*H][Npad][d] unscaled dQ accumulator
 struct BwdWorkspace {
-  float* lse2;
+  float* neg_lse2;
   float* delta;
   float* dqacc;
 };

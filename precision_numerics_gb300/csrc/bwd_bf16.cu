@@ -11,7 +11,7 @@
 //   dK      = scale dS^T Q,   dQ = scale dS K
 //
 // Three kernels, in stream order:
-//   1. preprocess   delta, LSE * log2(e) (+inf on padded rows, so the
+//   1. preprocess   delta, -LSE * log2(e) (-inf on padded rows, so the
 //                   recomputed P of a padded query row is exactly 0), and a
 //                   zeroed FP32 dQ accumulator.  Memory-bound.
 //   2. main         one CTA per (b, h, 128-key tile j), K_j and V_j resident in
@@ -39,6 +39,8 @@
 // thread execute in order).
 #include <math.h>
 
+#include <type_traits>
+
 #include "attn_internal.h"
 #include "ptx.cuh"
 
@@ -58,7 +60,7 @@ __device__ __forceinline__ void set_fail(unsigned int code) { atomicOr(&g_status
 template <int D>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                          const float* __restrict__ lse, float* __restrict__ lse2,
+                          const float* __restrict__ lse, float* __restrict__ neg_lse2,
                           float* __restrict__ delta, float4* __restrict__ dqacc, int N, int Npad) {
   constexpr int kGroup = D / 8;
   constexpr int kRows = 256 / kGroup;
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(256)
   const size_t prow = (size_t)bh * Npad + row;
   if (part == 0) {
     delta[prow] = s;
-    lse2[prow] = row < N ? lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
+    neg_lse2[prow] = row < N ? -(lse[(size_t)bh * N + row] * 1.4426950408889634f) : -INFINITY;
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   dqacc[prow * (D / 4) + 2 * part] = z;
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
-                    const float* __restrict__ lse2, const float* __restrict__ delta,
+                    const float* __restrict__ neg_lse2, const float* __restrict__ delta,
                     float* __restrict__ dqacc, int BH, int N, int Npad, float scale,
                     float scale_log2) {
   using C = BwdCfg<D>;
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       i * kBlockM, bh);
         }
         const size_t prow = (size_t)bh * Npad + (size_t)i * kBlockM;
-        bulk_load(sLse + st * 128, lse2 + prow, 512, &bar_qfull[st]);
+        bulk_load(sLse + st * 128, neg_lse2 + prow, 512, &bar_qfull[st]);
         bulk_load(sDelta + st * 128, delta + prow, 512, &bar_qfull[st]);
         issued = it + 1;
       }
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) reg_fence(p[c]);
       const float* L2 = sLse + st * 128;
       // Keys after the query (diagonal tile only) and padded keys get P = 0;
-      // padded queries have LSE*log2(e) = +inf, so their P is 0 already.
+      // padded queries have -LSE*log2(e) = -inf, so their P is 0 already.
       const int vis_from = (CAUSAL && i == j) ? r : 0;  // query columns c >= vis_from visible
 #pragma unroll
       for (int c = 0; c < 128; c += 4) {
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int cc = c + e;
-          float pv = ex2(fmaf(__uint_as_float(p[cc >> 5][cc & 31]), scale_log2, -lv[e]));
+          float pv = ex2(fmaf(__uint_as_float(p[cc >> 5][cc & 31]), scale_log2, lv[e]));
           if (!key_valid || cc < vis_from) pv = 0.f;
           p[cc >> 5][cc & 31] = __float_as_uint(pv);
         }
@@ -554,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // sub-partition has two warps to overlap the exp, TMEM and reduction latency.
 // TMEM (512 columns): dV [0,128), dK [128,256), S buffers [256,320) and
 // [320,384), dP [384,448), dQ^T [448,512).  Shared memory: K_j, V_j (32 KB
-// each), a 3-stage ring of Q_i / dO_i (16 KB each) with LSE*log2(e) and delta,
+// each), a 3-stage ring of Q_i / dO_i (16 KB each) with -LSE*log2(e) and delta,
 // and two dS^T buffers (16 KB each).  Each barrier that a role waits on is
 // either completed once per tile or split per buffer, so no waiter can fall
 // two phases behind the barrier it polls.
@@ -594,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmDO,  // box 64 rows
                          const __grid_constant__ CUtensorMap tmDK,  // box 128 rows
                          const __grid_constant__ CUtensorMap tmDV,  // box 128 rows
-                         const float* __restrict__ lse2, const float* __restrict__ delta,
+                         const float* __restrict__ neg_lse2, const float* __restrict__ delta,
                          float* __restrict__ dqacc, int BH, int N, int Npad, float scale,
                          float scale_log2) {
   constexpr int D = 128;
@@ -695,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       bh);
         }
         const size_t prow = (size_t)bh * Npad + (size_t)i * kBM;
-        bulk_load(sLse + st * kBM, lse2 + prow, kBM * 4, &bar_qfull[st]);
+        bulk_load(sLse + st * kBM, neg_lse2 + prow, kBM * 4, &bar_qfull[st]);
         bulk_load(sDelta + st * kBM, delta + prow, kBM * 4, &bar_qfull[st]);
         issued = it + 1;
       }
@@ -809,6 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kv = j * kBlockN + r;
     const bool key_valid = kv < N;
     const uint32_t dsBase0 = smem_u32(sDS);
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = !abort_all;
     // dQ^T(itd), query columns [32h, 32h+32): lane r adds head dim r of 32 query
     // rows; a warp's 32 reductions cover 128 contiguous bytes of one row.
@@ -843,21 +846,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence(p);
       const float* L2 = sLse + st * kBM + h * 32;
-      // Local column c is query i*64 + 32h + c.  Causal: it sees this key only
-      // when c >= vis_to.  Padded keys see nothing; padded queries have
-      // LSE*log2(e) = +inf, so their P is 0 already.
+      // P = exp2(c s - LSE log2 e), the argument of each column pair in one
+      // packed FP32 fma (bit-identical to two scalar fmas).  Local column c is
+      // query i*64 + 32h + c.  Causal: it sees this key only when c >= vis_to;
+      // padded keys see nothing.  Only tiles that cross the diagonal or hold
+      // padded keys take the masked loop.  Padded queries have
+      // -LSE log2(e) = -inf, so their P is 0 already.
       const int vis_to = CAUSAL ? kv - i * kBM - h * 32 : 0;
+      const bool need_mask =
+          (CAUSAL && i * kBM < (j + 1) * kBlockN) || (j + 1) * kBlockN > N;
+      auto p_block = [&](auto masked) {
 #pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
+          const uint64_t l2[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = c + e;
-          float pv = ex2(fmaf(__uint_as_float(p[cc]), scale_log2, -lv[e]));
-          if (!key_valid || cc < vis_to) pv = 0.f;
-          p[cc] = __float_as_uint(pv);
+          for (int e = 0; e < 4; e += 2) {
+            const int cc = c + e;
+            float x0, x1;
+            f2_unpack(fma2(f2_pack(__uint_as_float(p[cc]), __uint_as_float(p[cc + 1])), c2,
+                           l2[e >> 1]),
+                      x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if (decltype(masked)::value) {
+              if (!key_valid || cc < vis_to) p0 = 0.f;
+              if (!key_valid || cc + 1 < vis_to) p1 = 0.f;
+            }
+            p[cc] = __float_as_uint(p0);
+            p[cc + 1] = __float_as_uint(p1);
+          }
         }
+      };
+      if (need_mask) {
+        p_block(std::true_type{});
+      } else {
+        p_block(std::false_type{});
       }
       {
         uint32_t pk[16];
@@ -885,11 +908,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence(dp);
         uint32_t pk[16];
+        // dS = P o (dP - delta): dP - delta as fma(delta, -1, dP) (exact
+        // negation, one rounding: the subtraction), then the product, both packed.
+        const uint64_t m1 = f2_pack(-1.f, -1.f);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float2 d2 = *reinterpret_cast<const float2*>(Dl + 2 * e);
-          const float ds0 = __uint_as_float(p[2 * e]) * (__uint_as_float(dp[2 * e]) - d2.x);
-          const float ds1 = __uint_as_float(p[2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - d2.y);
+          const uint64_t diff = fma2(f2_pack(d2.x, d2.y), m1,
+                                     f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])));
+          float ds0, ds1;
+          f2_unpack(mul2(f2_pack(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])), diff),
+                    ds0, ds1);
           pk[e] = pack_bf16x2(ds0, ds1);
         }
         tmem_st16(tDP + h * 32, pk);  // inside this warpgroup's own dP columns
@@ -974,7 +1003,7 @@ cudaError_t preprocess_impl(const Problem& p, const void* o, const void* dout, c
   const int Npad = n_pad(p.N);
   dim3 grid(ceil_div(Npad, kRows), p.B * p.H);
   bwd_preprocess_kernel<D><<<grid, 256, 0, stream>>>(
-      static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, ws.lse2, ws.delta,
+      static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, ws.neg_lse2, ws.delta,
       reinterpret_cast<float4*>(ws.dqacc), p.N, Npad);
   return cudaGetLastError();
 }
@@ -1002,7 +1031,7 @@ cudaError_t main_impl(const Problem& p, const CUtensorMap* maps, const BwdWorksp
   const int Npad = n_pad(p.N);
   const int n_kt = Npad / kBlockN;
   kernel<<<dim3(BH * n_kt), dim3(kThreads), C::kSmemBytes, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.lse2, ws.delta, ws.dqacc, BH, p.N,
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.neg_lse2, ws.delta, ws.dqacc, BH, p.N,
       Npad, p.scale, p.scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
@@ -1018,7 +1047,7 @@ cudaError_t main_d128_impl(const Problem& p, const CUtensorMap* maps, const BwdW
   const int Npad = n_pad(p.N);
   const int n_kt = Npad / kBlockN;
   kernel<<<dim3(BH * n_kt), dim3(kThreads), r64::kSmemBytes, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.lse2, ws.delta, ws.dqacc, BH, p.N,
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.neg_lse2, ws.delta, ws.dqacc, BH, p.N,
       Npad, p.scale, p.scale * 1.4426950408889634f);
   return cudaGetLastError();
 }

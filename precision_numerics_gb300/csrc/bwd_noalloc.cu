@@ -6,7 +6,7 @@
 // whole device-memory budget and hands out only the tensors it manages, or a
 // latency-critical loop where cudaMalloc/cudaFree (and the implicit
 // synchronization they can bring) is not acceptable.  Such callers still
-// pass their inputs and outputs; the backward's scratch (LSE*log2(e), delta
+// pass their inputs and outputs; the backward's scratch (-LSE*log2(e), delta
 // and the FP32 dQ accumulator) comes from g_bwd_scratch below.
 //
 // Costs and rules of use:
@@ -19,7 +19,7 @@
 //    race on it and produce wrong results; serialise them.
 //  * The array keeps the previous call's contents.  Every call rewrites all
 //    of the part it uses before reading it: the preprocess kernel writes
-//    LSE*log2(e) and delta for every padded row and zeroes the dQ
+//    -LSE*log2(e) and delta for every padded row and zeroes the dQ
 //    accumulator.
 //  * The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress while that device is current; make that first call
