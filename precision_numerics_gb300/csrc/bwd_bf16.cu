@@ -353,17 +353,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Keys after the query (diagonal tile only) and padded keys get P = 0;
       // padded queries have -LSE*log2(e) = -inf, so their P is 0 already.
       const int vis_from = (CAUSAL && i == j) ? r : 0;  // query columns c >= vis_from visible
+      // Packed FP32 pair fma for the argument (bit-identical to scalar fmas);
+      // only the diagonal tile and a tile with padded keys take the masked loop.
+      const bool need_mask = (CAUSAL && i == j) || (j + 1) * kBlockN > N;
+      const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+      auto p_block = [&](auto masked) {
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int c = 0; c < 128; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
+          const uint64_t l2[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = c + e;
-          float pv = ex2(fmaf(__uint_as_float(p[cc >> 5][cc & 31]), scale_log2, lv[e]));
-          if (!key_valid || cc < vis_from) pv = 0.f;
-          p[cc >> 5][cc & 31] = __float_as_uint(pv);
+          for (int e = 0; e < 4; e += 2) {
+            const int cc = c + e;
+            float x0, x1;
+            f2_unpack(fma2(f2_pack(__uint_as_float(p[cc >> 5][cc & 31]),
+                                   __uint_as_float(p[cc >> 5][(cc & 31) + 1])),
+                           c2, l2[e >> 1]),
+                      x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if (decltype(masked)::value) {
+              if (!key_valid || cc < vis_from) p0 = 0.f;
+              if (!key_valid || cc + 1 < vis_from) p1 = 0.f;
+            }
+            p[cc >> 5][cc & 31] = __float_as_uint(p0);
+            p[cc >> 5][(cc & 31) + 1] = __float_as_uint(p1);
+          }
         }
+      };
+      if (need_mask) {
+        p_block(std::true_type{});
+      } else {
+        p_block(std::false_type{});
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -393,12 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence(dp);
         uint32_t pk[16];
+        // dS = P o (dP - delta), packed: the difference as fma(delta, -1, dP).
+        const uint64_t m1 = f2_pack(-1.f, -1.f);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c0 = c * 32 + 2 * e;
           const float2 d2 = *reinterpret_cast<const float2*>(Dl + c0);
-          const float ds0 = __uint_as_float(p[c][2 * e]) * (__uint_as_float(dp[2 * e]) - d2.x);
-          const float ds1 = __uint_as_float(p[c][2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - d2.y);
+          const uint64_t diff = fma2(f2_pack(d2.x, d2.y), m1,
+                                     f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])));
+          float ds0, ds1;
+          f2_unpack(mul2(f2_pack(__uint_as_float(p[c][2 * e]), __uint_as_float(p[c][2 * e + 1])), diff),
+                    ds0, ds1);
           pk[e] = pack_bf16x2(ds0, ds1);
         }
         tmem_st16(tDP + c * 16, pk);
@@ -552,8 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dQ^T puts head-dim index d on the TMEM lanes: each drain thread owns one d,
 // and a warp's 32 reductions into the FP32 accumulator cover 128 contiguous
 // bytes of one query row.  Warps 4-11 form two warpgroups that split every
-// tile's 64 query columns (P, dS and the dQ drain) between them, so each SM
-// sub-partition has two warps to overlap the exp, TMEM and reduction latency.
+// tile's 64 query columns (P and dS) between them, so each SM sub-partition
+// has two warps to overlap the exp and TMEM latency; warps 12-15 drain dQ^T
+// into the accumulator, so the reductions' issue stalls stay off the P / dS
+// path.
 // TMEM (512 columns): dV [0,128), dK [128,256), S buffers [256,320) and
 // [320,384), dP [384,448), dQ^T [448,512).  Shared memory: K_j, V_j (32 KB
 // each), a 3-stage ring of Q_i / dO_i (16 KB each) with -LSE*log2(e) and delta,
@@ -563,6 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace r64 {
 
 constexpr int kBM = 64;                    // query rows per tile
+constexpr int kThreadsR = 512;             // + warps 12-15: dQ drain
+constexpr int kRegsWG0 = 96, kRegsCompute = 168, kRegsDrain = 80;  // setmaxnreg split
+static_assert(kRegsWG0 + 2 * kRegsCompute + kRegsDrain <= 512, "split exceeds the launch pool");
 constexpr int kStages = 3;                 // Q / dO ring depth
 constexpr int kKVBytes = 128 * 128 * 2;    // K_j or V_j (128 rows x 128 d)
 constexpr int kKVChunk = 128 * 128;        // one 64-column chunk of K_j / V_j
@@ -589,7 +619,7 @@ constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ =
 __host__ __device__ constexpr uint32_t packed_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
 
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsR, 1)
     bwd_main_d128_kernel(const __grid_constant__ CUtensorMap tmQ,   // box 64 rows
                          const __grid_constant__ CUtensorMap tmK,   // box 128 rows
                          const __grid_constant__ CUtensorMap tmV,   // box 128 rows
@@ -646,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_dpfull, 1);
     mbar_init(bar_dsready, 256);
     mbar_init(bar_dqfull, 1);
-    mbar_init(bar_dqfree, 256);
+    mbar_init(bar_dqfree, 128);
     mbar_init(bar_dkvdone, 1);
     mbar_init(bar_final, 1);
     mbar_init(bar_epi_dv, 128);
@@ -672,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sDelta = reinterpret_cast<float*>(smem + kOffDelta);
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG0));
     if (warp == 0 && lane == 0 && !abort_all) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&tmQ);
@@ -794,44 +824,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_final, 0);
     }
     __syncwarp();
+  } else if (warp >= 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDrain));
+    // ------------------------------------------------------------ dQ drain
+    // dQ^T(it), all 64 query columns: lane r adds head dim r of each query row;
+    // a warp's 32 reductions of one column cover 128 contiguous bytes.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tDQ = tmem + lane_off + kColDQ;
+    bool ok = !abort_all;
+    for (int itd = 0; itd < nq && ok; ++itd) {
+      ok = warp_wait(bar_dqfull, itd & 1);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t acc[2][32];
+      tmem_ld32(tDQ, acc[0]);
+      tmem_ld32(tDQ + 32, acc[1]);
+      tmem_wait_ld();
+      reg_fence(acc[0]);
+      reg_fence(acc[1]);
+      tc_fence_before();
+      mbar_arrive(bar_dqfree);
+      float* dst = dqacc + ((size_t)bh * Npad + (size_t)(i_first + itd) * kBM) * D + r;
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)c * D),
+                     "f"(__uint_as_float(acc[c >> 5][c & 31]))
+                     : "memory");
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
-    // ------------------------------- P, dS and the dQ drain (two warpgroups)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
+    // ------------------------------------------- P and dS (two warpgroups)
     // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) owns query columns
     // [32h, 32h+32) of every 64-row tile: it computes those columns of P^T
-    // and dS^T (thread = key row = TMEM lane) and drains those columns of
-    // dQ^T (thread = head dim = TMEM lane).  The drain of dQ^T(it-1) runs at
-    // the end of iteration it, after dS(it); dQ^T(it) needs dS(it), so the
-    // drain is never more than one product behind.
+    // and dS^T (thread = key row = TMEM lane).
     const int h = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tDP = tmem + lane_off + kColDP;
-    const uint32_t tDQ = tmem + lane_off + kColDQ + h * 32;
     const int kv = j * kBlockN + r;
     const bool key_valid = kv < N;
     const uint32_t dsBase0 = smem_u32(sDS);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = !abort_all;
-    // dQ^T(itd), query columns [32h, 32h+32): lane r adds head dim r of 32 query
-    // rows; a warp's 32 reductions cover 128 contiguous bytes of one row.
-    auto drain = [&](int itd) -> bool {
-      if (!warp_wait(bar_dqfull, itd & 1)) return false;
-      tc_fence_after();
-      uint32_t acc[32];
-      tmem_ld32(tDQ, acc);
-      tmem_wait_ld();
-      reg_fence(acc);
-      tc_fence_before();
-      mbar_arrive(bar_dqfree);
-      float* dst = dqacc + ((size_t)bh * Npad + (size_t)(i_first + itd) * kBM + h * 32) * D + r;
-#pragma unroll
-      for (int c = 0; c < 32; ++c)
-        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)c * D),
-                     "f"(__uint_as_float(acc[c]))
-                     : "memory");
-      return true;
-    };
     for (int it = 0; it < nq && ok; ++it) {
       const int st = it % kStages, b = it & 1;
       const int i = i_first + it;
@@ -936,11 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar_dsready);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_qempty[st]);
-      // dQ^T(it-1) is done or nearly so; the MMA warp needs dq_free only after
-      // it has issued dK(it) and dP^T(it+1).
-      if (it > 0) ok = drain(it - 1);
     }
-    if (ok && !abort_all) ok = drain(nq - 1);
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
     // ------------------------- epilogue: h = 0 stores dV, h = 1 stores scale*dK
     if (ok && !abort_all) {
@@ -1046,7 +1078,7 @@ cudaError_t main_d128_impl(const Problem& p, const CUtensorMap* maps, const BwdW
   const int BH = p.B * p.H;
   const int Npad = n_pad(p.N);
   const int n_kt = Npad / kBlockN;
-  kernel<<<dim3(BH * n_kt), dim3(kThreads), r64::kSmemBytes, stream>>>(
+  kernel<<<dim3(BH * n_kt), dim3(r64::kThreadsR), r64::kSmemBytes, stream>>>(
       maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.neg_lse2, ws.delta, ws.dqacc, BH, p.N,
       Npad, p.scale, p.scale * 1.4426950408889634f);
   return cudaGetLastError();
