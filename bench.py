@@ -14,7 +14,7 @@ Rank 0 prints ONE JSON line.  `value` is whole-job TFLOP/s with inputs
 resident in HBM; `e2e` is the same metric measured through the Python API
 with pinned host buffers (host->device copies of Q, K, V, dO and
 device->host copies of O, LSE, dQ, dK, dV inside the timed region);
-(HostAttention pipelines head groups over three streams); `roofline` describes the dominant kernel (the backward main kernel) timed
+(HostAttention pipelines head groups over upload, compute and download streams, replayed as a CUDA graph); `roofline` describes the dominant kernel (the backward main kernel) timed
 with CUDA events on its stream; `cpu_baseline` is the FP64 oracle timed on
 the host cores on a bounded sample.  `--impl reference` times that oracle
 as the reference arm instead.  Under torchrun every rank runs its own full
@@ -300,7 +300,8 @@ def run_ours(args, w):
     attn.attn_check_status()
 
     # End-to-end through the public API with pinned host buffers: the head
-    # groups are pipelined (H2D copy, kernels, D2H copy on three streams).
+    # groups are pipelined (H2D copy, kernels, D2H copy on their own streams),
+    # captured once as a CUDA graph and replayed every step.
     from precision_numerics_gb300.host import HostAttention
     pipe = HostAttention(B, H, N, d, scale=w.scale, causal=w.causal, chunks=args.e2e_chunks,
                          device=dev)

@@ -262,10 +262,13 @@ def test_stable_forward_caps_the_shift_for_huge_repeated_maxima(A):
                  backward=False)
 
 
-@pytest.mark.parametrize("chunks", [1, 3])
-def test_host_pipeline_matches_device_path(A, chunks):
-    """HostAttention (pinned host buffers, head groups pipelined over three
-    streams) gives the device path's results; run twice to exercise reuse."""
+@pytest.mark.parametrize("chunks,group_sizes,streams,graph",
+                         [(1, None, 1, True), (3, None, 1, True), (3, None, 1, False),
+                          (0, [1, 3, 1], 2, True), (0, [2, 3], 2, False)])
+def test_host_pipeline_matches_device_path(A, chunks, group_sizes, streams, graph):
+    """HostAttention (pinned host buffers, head groups pipelined over upload,
+    compute and download streams, eagerly or as a replayed CUDA graph) gives
+    the device path's results; run twice to exercise buffer and graph reuse."""
     from precision_numerics_gb300.host import HostAttention
     B, H, N, d = 1, 5, 300, 128
     x = inputs.random_qkv(10, B, H, N, d)
@@ -273,7 +276,8 @@ def test_host_pipeline_matches_device_path(A, chunks):
     t = {k: v.cuda() for k, v in host.items()}
     o, lse = A.attn_fwd(t["q"], t["k"], t["v"], causal=True)
     dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=True)
-    pipe = HostAttention(B, H, N, d, causal=True, chunks=chunks)
+    pipe = HostAttention(B, H, N, d, causal=True, chunks=chunks or 4, group_sizes=group_sizes,
+                         compute_streams=streams, graph=graph)
     for _ in range(2):
         ho, hl, hdq, hdk, hdv = pipe.run(host["q"], host["k"], host["v"], host["do"])
         torch.cuda.synchronize()
@@ -282,3 +286,30 @@ def test_host_pipeline_matches_device_path(A, chunks):
         assert torch.equal(hdk, dk.cpu()) and torch.equal(hdv, dv.cpu())
         rel = float((hdq.float() - dq.float().cpu()).norm() / dq.float().cpu().norm())
         assert rel <= 1e-2
+
+
+def test_host_pipeline_rejects_bad_group_sizes(A):
+    from precision_numerics_gb300.host import HostAttention
+    with pytest.raises(ValueError):
+        HostAttention(1, 4, 128, 64, group_sizes=[2, 1])
+    with pytest.raises(ValueError):
+        HostAttention(1, 4, 128, 64, group_sizes=[4, 0])
+
+
+def test_host_pipeline_graph_follows_new_input_buffers(A):
+    """A graph-mode pipeline re-captures when it is handed other host tensors."""
+    from precision_numerics_gb300.host import HostAttention
+    B, H, N, d = 1, 2, 256, 64
+    pipe = HostAttention(B, H, N, d, causal=False, chunks=2)
+    outs = []
+    for seed in (3, 4):
+        x = inputs.random_qkv(seed, B, H, N, d)
+        host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+                for k, v in x.items()}
+        ho = pipe.run(host["q"], host["k"], host["v"], host["do"])[0]
+        torch.cuda.synchronize()
+        t = {k: v.cuda() for k, v in host.items()}
+        o, _ = A.attn_fwd(t["q"], t["k"], t["v"], causal=False)
+        assert torch.equal(ho, o.cpu())
+        outs.append(ho.clone())
+    assert not torch.equal(outs[0], outs[1])
