@@ -23,8 +23,10 @@
 //                     dV  += P^T dO_i             (TS, P^T in TMEM)
 //                     dK  += dS^T Q_i             (TS, dS^T in TMEM)
 //                     dQ_i = dS K_j               (SS, dS from shared memory)
-//                   and dQ_i is added into the FP32 accumulator with vector
-//                   reductions.  Warp roles: 0 TMA producer, 1 MMA issuer,
+//                   and dQ_i is added into the FP32 accumulator with
+//                   red.global.add.f32 (a warp's 32 reductions cover 128
+//                   contiguous bytes).  Warp roles (d = 64 variant; the d = 128
+//                   one is described at r64): 0 TMA producer, 1 MMA issuer,
 //                   2 TMEM owner, 4-7 P / dS compute (one key row per thread),
 //                   8-11 dQ drain; the epilogue writes dV (warps 4-7) and
 //                   scale * dK (warps 8-11) with TMA stores.

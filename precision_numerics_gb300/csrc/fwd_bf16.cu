@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c >= lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
       // Row max as four independent chains of three-input maxima (short
-      // dependency chains: only two softmax warps share an SM sub-partition).
+      // dependency chains: few warps share an SM sub-partition to hide them).
       float mx4[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
