@@ -397,8 +397,9 @@ def run_deviation(args):
     """Numeric-deviation report, one JSON line per workload (head (0,0)).
 
     For O, LSE, dQ, dK, dV: the tiled GPU kernel, the tiled GPU kernel with
-    the stabilised normaliser (beta = 2), and the naive BF16 attention, each
-    against the FP64 definition.  Also delta = rowsum(dO o O) formed from the
+    the stabilised normaliser (beta = 2; on the exact-tie workload also beta =
+    1.05, 1.5 and 4), and the naive BF16 attention, each against the FP64
+    definition.  Also delta = rowsum(dO o O) formed from the
     GPU's BF16 O (delta_lp, what the backward uses) against delta from the
     exact O ("Why Low-Precision Transformer Training Fails", Figure 3).
     """
@@ -417,8 +418,14 @@ def run_deviation(args):
         x = inputs.make_inputs(w, seed=0, sigma=sigma)
         t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in x.items()}
         runs = {}
-        for tag, fwd in (("tiled_gpu", attn.attn_fwd),
-                         ("tiled_gpu_stable", lambda *a, **kw: attn.attn_fwd_stable(*a, beta=2.0, **kw))):
+        variants = [("tiled_gpu", attn.attn_fwd),
+                    ("tiled_gpu_stable", lambda *a, **kw: attn.attn_fwd_stable(*a, beta=2.0, **kw))]
+        if w.tied_keys:
+            # beta is not legible on the pages: sweep it where maxima repeat exactly
+            for beta in (1.05, 1.5, 4.0):
+                variants.append((f"tiled_gpu_stable_beta{beta:g}",
+                                 lambda *a, _b=beta, **kw: attn.attn_fwd_stable(*a, beta=_b, **kw)))
+        for tag, fwd in variants:
             o, lse = fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
             g = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale, causal=w.causal)
             attn.attn_check_status()
