@@ -84,6 +84,12 @@ class HostAttention:
 
     def run(self, q, k, v, do):
         """Enqueue the whole pipeline; the current stream waits for its end."""
+        shape = (self.B, self.H, self.N, self.d)
+        for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
+            if x.device.type != "cpu" or not x.is_pinned():
+                raise ValueError(f"{name} must be a pinned host tensor (tensor.pin_memory())")
+            if tuple(x.shape) != shape or x.dtype != torch.bfloat16 or not x.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous BF16 tensor of shape {shape}")
         if not self.graph:
             return self._enqueue(q, k, v, do, after_previous=True)
         key = (q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr())

@@ -303,6 +303,18 @@ def test_host_pipeline_rejects_bad_group_sizes(A):
         HostAttention(1, 4, 128, 64, group_sizes=[4, 0])
 
 
+def test_host_pipeline_rejects_unpinned_or_misshaped_inputs(A):
+    from precision_numerics_gb300.host import HostAttention
+    pipe = HostAttention(1, 2, 128, 64, chunks=2)
+    good = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(ValueError):
+        pipe.run(torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16), good, good, good)
+    with pytest.raises(ValueError):
+        pipe.run(good.cuda(), good, good, good)
+    with pytest.raises(ValueError):
+        pipe.run(torch.zeros(1, 2, 64, 64, dtype=torch.bfloat16).pin_memory(), good, good, good)
+
+
 def test_host_pipeline_graph_follows_new_input_buffers(A):
     """A graph-mode pipeline re-captures when it is handed other host tensors."""
     from precision_numerics_gb300.host import HostAttention
