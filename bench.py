@@ -167,11 +167,25 @@ def _traffic_per_launch(workload: str):
 # ---------------------------------------------------------------------------
 # CPU oracle (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-def _oracle_head_step(w, x, head):
+def _oracle_head_step(w, x, head, rows=None):
+    """Oracle forward + backward for the first `rows` query rows of one head.
+
+    With a causal mask the first R rows see only the first R keys, so the
+    sample is exactly the square problem of size R; without the mask they see
+    all N keys.  rows = None (or N) is the whole head.
+    """
     import oracle
+    R = w.N if rows is None else rows
     f = {k: inputs.bf16_bits_to_f32(v.reshape(w.B * w.H, w.N, w.d)[head]) for k, v in x.items()}
-    oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
-    oracle.backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)
+    nk = R if w.causal else w.N
+    oracle.forward(f["q"][:R], f["k"][:nk], f["v"][:nk], w.scale, w.causal)
+    oracle.backward(f["q"][:R], f["k"][:nk], f["v"][:nk], f["do"][:R], w.scale, w.causal)
+
+
+def _rows_flops(w, rows):
+    """Forward + backward FLOPs of the first `rows` query rows of one head."""
+    pairs = rows * rows / 2 if w.causal else rows * w.N  # (query, key) pairs computed
+    return 3.5 * 4 * pairs * w.d
 
 
 def _head_flops(w):
@@ -201,19 +215,30 @@ def cpu_baseline(w, x, budget_s=12.0):
                       f"{dt:.1f} s; throughput scales linearly with heads"}
 
 
-def run_reference(args, w):
+def run_reference(args, w, budget_s=150.0):
     world, rank, _ = _dist()
     if rank != 0:
         return 0
     x = inputs.make_inputs(w, seed=0, heads=None)
+    # One step = the oracle on one head; when K such steps would not end within
+    # ~budget_s, each step takes the first R query rows of a head instead, R
+    # sized from a timed whole head so that K steps fit the budget.
+    t0 = time.perf_counter()
+    _oracle_head_step(w, x, 0)
+    t_head = time.perf_counter() - t0
+    rows = w.N
+    if args.steps * t_head > budget_s:
+        frac = budget_s / (args.steps * t_head)
+        rows = max(64, int(w.N * (frac ** 0.5 if w.causal else frac)))
     for s in range(args.warmup):
-        _oracle_head_step(w, x, s % (w.B * w.H))
+        _oracle_head_step(w, x, s % (w.B * w.H), rows)
     t0 = time.perf_counter()
     for s in range(args.steps):
-        _oracle_head_step(w, x, s % (w.B * w.H))
+        _oracle_head_step(w, x, s % (w.B * w.H), rows)
     dt = time.perf_counter() - t0
-    value = args.steps * _head_flops(w) / dt / 1e12
-    sample = f"each step = 1 of {w.B * w.H} (b,h) heads of {w.name}, FP64 forward+backward"
+    value = args.steps * _rows_flops(w, rows) / dt / 1e12
+    sample = (f"each step = the first {rows} of {w.N} query rows of one of the {w.B * w.H} (b,h) "
+              f"heads of {w.name}, FP64 forward+backward")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
