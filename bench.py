@@ -2,7 +2,7 @@
 """Benchmark of the BF16 attention hot path (forward + backward) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama7b] [--deviation]
+                    [--workload llama7b] [--deviation] [--int8-forward]
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 attn_fwd (O, LSE) then the backward (preprocess, main kernel, dQ conversion).
@@ -477,6 +477,70 @@ def run_deviation(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# INT8-input forward (per-token INT8 Q and K, BF16 V)
+# ---------------------------------------------------------------------------
+def run_int8_forward(args, w):
+    """One JSON line for the INT8-input forward: a step quantizes Q and K
+    (attn_quantize_int8) and runs attn_fwd_int8; value = forward FLOP count
+    (4*B*H*N^2*d, halved when causal) per second.  Next to it: the BF16
+    forward's time, and both forwards' deviation from the FP64 definition on
+    head (0,0) (the INT8 one also against the INT8 oracle)."""
+    import torch
+
+    import oracle
+    from oracle import int8 as oi
+    from precision_numerics_gb300 import attn, build
+    from precision_numerics_gb300.deviation import deviation
+
+    build.build()
+    x = inputs.make_inputs(w, seed=0)
+    t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in x.items()}
+    q8, qs = attn.attn_quantize_int8(t["q"])
+    k8, ks = attn.attn_quantize_int8(t["k"])
+    o8, l8 = attn.attn_fwd_int8(q8, qs, k8, ks, t["v"], scale=w.scale, causal=w.causal)
+    ob, lb = attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        attn.attn_quantize_int8(t["q"], q8, qs)
+        attn.attn_quantize_int8(t["k"], k8, ks)
+        attn.attn_fwd_int8(q8, qs, k8, ks, t["v"], scale=w.scale, causal=w.causal, o=o8, lse=l8)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(1, min(args.steps, 200))
+    ms = timed(step, steps)
+    ms_bf16 = timed(lambda: attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal,
+                                          o=ob, lse=lb), steps)
+    attn.attn_check_status()
+    f = {k: inputs.bf16_bits_to_f32(v.reshape(w.B * w.H, w.N, w.d)[0]) for k, v in x.items()}
+    o_ref, _ = oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+    o_i8ref, _ = oi.int8_forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+    o8h = o8.reshape(w.B * w.H, w.N, w.d)[0].float().cpu().numpy()
+    obh = ob.reshape(w.B * w.H, w.N, w.d)[0].float().cpu().numpy()
+    line = {"metric": "INT8-input attention forward TFLOP/s-equivalent on 1 GB300",
+            "value": w.fwd_flops() / ms / 1e9, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "s8 (Q K^T), bf16 (P V)", "data": "synthetic", "config": _config(w),
+            "step": "attn_quantize_int8 on Q and K + attn_fwd_int8",
+            "bf16_forward": {"ms": ms_bf16, "tflops": w.fwd_flops() / ms_bf16 / 1e9},
+            "o_vs_fp64": {"int8": deviation(o8h, o_ref), "bf16": deviation(obh, o_ref)},
+            "o_int8_vs_int8_oracle": deviation(o8h, o_i8ref)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,6 +548,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama7b", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--int8-forward", action="store_true",
+                    help="print the INT8-input forward line instead of the bench line")
     ap.add_argument("--deviation", action="store_true",
                     help="print the numeric-deviation report instead of the bench line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -494,6 +560,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.deviation:
         return run_deviation(args)
+    if args.int8_forward:
+        return run_int8_forward(args, inputs.WORKLOADS[args.workload])
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -106,6 +106,38 @@ ATTN_API attn_status attn_fwd_stable(const void* q, const void* k, const void* v
                                      int causal, float beta, attn_dtype dt, cudaStream_t stream);
 
 /*
+ * Per-token symmetric INT8 quantization ("INT-FlashAttention: Enabling Flash
+ * Attention for INT8 Quantization", abstract; the page fixes no scheme, the
+ * one here is a reading): for every row r of every head of the BF16 tensor
+ * x [B,H,N,d], scales[r] = max_j |x_rj| / 127 (FP32) and codes[r][j] =
+ * rint(x_rj / scales[r]) clamped to [-127, 127], rint rounding half to even;
+ * a row of zeros gets scale 0 and codes 0.
+ *   x      : [B,H,N,d] BF16, device.
+ *   codes  : [B,H,N,d] int8, device, written.
+ *   scales : [B,H,N] FP32, device, written.
+ * d in {64, 128}; all pointers 16-byte aligned.
+ */
+ATTN_API attn_status attn_quantize_int8(const void* x, void* codes, float* scales, int B, int H,
+                                        int N, int d, cudaStream_t stream);
+
+/*
+ * Forward on per-token INT8 Q and K (as written by attn_quantize_int8) and
+ * BF16 V: S_ij = scale * q_scale[i] * k_scale[j] * (q8_i . k8_j) with the
+ * integer dot product exact, then the FP32 online softmax and P V (P rounded
+ * to BF16), O = softmax(S [+mask]) V and LSE = ln sum_j exp(S_ij) as in
+ * attn_fwd.  sm_103a has no INT8 tcgen05 MMA, so this path runs on the
+ * warp-level mma.sync tensor-core instructions and is slower than attn_fwd;
+ * it exists for the numerics of INT8 inputs.
+ *   q8, k8  : [B,H,N,d] int8, device.   q_scale, k_scale : [B,H,N] FP32.
+ *   v       : [B,H,N,d] BF16.           o : [B,H,N,d] BF16.   lse : [B,H,N] FP32.
+ * d in {64, 128}; all pointers 16-byte aligned, device memory.
+ */
+ATTN_API attn_status attn_fwd_int8(const void* q8, const float* q_scale, const void* k8,
+                                   const float* k_scale, const void* v, void* o, float* lse,
+                                   int B, int H, int N, int d, float scale, int causal,
+                                   cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (0 on invalid
  * arguments).  Layout (internal): -LSE*log2(e) and delta, FP32 [B*H][Npad]
  * each, and the FP32 dQ accumulator [B*H][Npad][d], Npad = N rounded up to

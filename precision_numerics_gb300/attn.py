@@ -24,7 +24,7 @@ ATTN_DTYPE_BF16, ATTN_DTYPE_FP32 = 0, 1
 EXPORTED = ("attn_version", "attn_status_string", "attn_last_error", "attn_fwd",
             "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
             "attn_bwd_dq_convert", "attn_check_status", "attn_selftest_wait_timeout",
-            "attn_bwd_noalloc", "attn_fwd_stable")
+            "attn_bwd_noalloc", "attn_fwd_stable", "attn_quantize_int8", "attn_fwd_int8")
 
 
 class AttnError(RuntimeError):
@@ -51,6 +51,8 @@ _SIGNATURES = {
     "attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
     "attn_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
     "attn_fwd_stable": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _f, _i, _vp]),
+    "attn_quantize_int8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "attn_fwd_int8": (_i, [_vp] * 7 + [_i, _i, _i, _i, _f, _i, _vp]),
 }
 
 
@@ -166,6 +168,42 @@ def attn_fwd_stable(q, k, v, scale=None, causal=False, beta=2.0, o=None, lse=Non
     _call("attn_fwd_stable", q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
           lse.data_ptr(), B, H, N, d, _default_scale(d, scale), int(bool(causal)), float(beta),
           ATTN_DTYPE_BF16, _stream(stream))
+    return o, lse
+
+
+def attn_quantize_int8(x, codes=None, scales=None, stream=None):
+    """Per-token symmetric INT8 codes and FP32 scales of a BF16 [B,H,N,d] tensor."""
+    _check_bhnd("x", x, dtype=torch.bfloat16)
+    B, H, N, d = x.shape
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scales is None:
+        scales = torch.empty((B, H, N), dtype=torch.float32, device=x.device)
+    _check_bhnd("codes", codes, x.shape, torch.int8)
+    _check_lse(scales, B, H, N)
+    _call("attn_quantize_int8", x.data_ptr(), codes.data_ptr(), scales.data_ptr(), B, H, N, d,
+          _stream(stream))
+    return codes, scales
+
+
+def attn_fwd_int8(q8, q_scale, k8, k_scale, v, scale=None, causal=False, o=None, lse=None,
+                  stream=None):
+    """Forward on per-token INT8 Q and K (attn_quantize_int8) and BF16 V.  Returns (o, lse)."""
+    _check_bhnd("v", v, dtype=torch.bfloat16)
+    B, H, N, d = v.shape
+    for name, t in (("q8", q8), ("k8", k8)):
+        _check_bhnd(name, t, v.shape, torch.int8)
+    _check_lse(q_scale, B, H, N)
+    _check_lse(k_scale, B, H, N)
+    if o is None:
+        o = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=v.device)
+    _check_bhnd("o", o, v.shape, v.dtype)
+    _check_lse(lse, B, H, N)
+    _call("attn_fwd_int8", q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
+          v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, _default_scale(d, scale),
+          int(bool(causal)), _stream(stream))
     return o, lse
 
 

@@ -58,6 +58,14 @@ cudaError_t launch_bwd_fp32(const Problem& p, const float* q, const float* k, co
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
 
+// INT8-input forward: per-token quantization of a BF16 [B,H,N,d] tensor, and
+// the forward on INT8 Q, K (with their per-row scales) and BF16 V.
+cudaError_t launch_quantize_int8(const Problem& p, const void* x, void* codes, float* scales,
+                                 cudaStream_t stream);
+cudaError_t launch_fwd_int8(const Problem& p, const void* q8, const float* qs, const void* k8,
+                            const float* ks, const void* v, void* o, float* lse,
+                            cudaStream_t stream);
+
 // Device status words (one per kernel translation unit): read and clear.
 cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream);
 cudaError_t read_and_clear_status_bwd(unsigned int* out, cudaStream_t stream);
