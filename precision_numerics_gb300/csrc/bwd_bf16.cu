@@ -63,11 +63,13 @@ template <int D>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                           const float* __restrict__ lse, float* __restrict__ neg_lse2,
-                          float* __restrict__ delta, float4* __restrict__ dqacc, int N, int Npad) {
+                          float* __restrict__ delta, float4* __restrict__ dqacc, int N, int Npad,
+                          int blocks_per_head) {
   constexpr int kGroup = D / 8;
   constexpr int kRows = 256 / kGroup;
-  const int bh = blockIdx.y;
-  const int row = blockIdx.x * kRows + threadIdx.x / kGroup;
+  // One-dimensional grid (B*H may exceed the 65535 limit of gridDim.y).
+  const int bh = (int)(blockIdx.x / (unsigned)blocks_per_head);
+  const int row = (int)(blockIdx.x % (unsigned)blocks_per_head) * kRows + threadIdx.x / kGroup;
   const int part = threadIdx.x % kGroup;
   const bool active = row < Npad;
   float s = 0.f;
@@ -1035,10 +1037,11 @@ cudaError_t preprocess_impl(const Problem& p, const void* o, const void* dout, c
                             const BwdWorkspace& ws, cudaStream_t stream) {
   constexpr int kRows = 256 / (D / 8);
   const int Npad = n_pad(p.N);
-  dim3 grid(ceil_div(Npad, kRows), p.B * p.H);
-  bwd_preprocess_kernel<D><<<grid, 256, 0, stream>>>(
+  const int per_head = ceil_div(Npad, kRows);
+  const unsigned blocks = (unsigned)per_head * (unsigned)(p.B * p.H);
+  bwd_preprocess_kernel<D><<<blocks, 256, 0, stream>>>(
       static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, ws.neg_lse2, ws.delta,
-      reinterpret_cast<float4*>(ws.dqacc), p.N, Npad);
+      reinterpret_cast<float4*>(ws.dqacc), p.N, Npad, per_head);
   return cudaGetLastError();
 }
 

@@ -17,6 +17,8 @@ import oracle
 from precision_numerics_gb300 import inputs
 from precision_numerics_gb300.deviation import deviation
 
+from bounds import delta_error_bound
+
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
@@ -71,3 +73,34 @@ def test_largest_accepted_problem(A):
     bound = 2.0 ** -8 * np.abs(f["do"]).sum(axis=0)
     assert np.all(np.abs(dv_sum - do_sum) <= bound)
     assert np.abs(dv_sum - do_sum).max() <= 0.05 * np.sqrt(N)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_more_heads_than_a_grid_y_dimension(A, causal):
+    """B*H = 70000 heads (above the 65535 limit of a grid's y dimension), short rows."""
+    B, H, N, d = 2, 35000, 3, 64
+    scale = d ** -0.5
+    x = inputs.random_qkv(12, B, H, N, d)
+    t = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).cuda()
+         for k, v in x.items()}
+    o, lse = A.attn_fwd(t["q"], t["k"], t["v"], scale=scale, causal=causal)
+    dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=scale, causal=causal)
+    A.attn_check_status()
+    for g in (o, dq, dk, dv):
+        assert bool(torch.isfinite(g.float()).all())
+    flat = {k: inputs.bf16_bits_to_f32(v).reshape(B * H, N, d) for k, v in x.items()}
+    got = {k: g.float().cpu().numpy().reshape(B * H, N, d)
+           for k, g in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv))}
+    lse_h = lse.cpu().numpy().reshape(B * H, N)
+    for h in (0, 34999, 35000, B * H - 1):
+        f = {k: v[h] for k, v in flat.items()}
+        o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], scale, causal)
+        g_ref = oracle.backward(f["q"], f["k"], f["v"], f["do"], scale, causal)
+        assert deviation(got["o"][h], o_ref)["max_abs"] <= 2e-2, h
+        assert np.abs(lse_h[h] - lse_ref).max() <= 1e-3, h
+        assert deviation(got["dv"][h], g_ref[2])["rel_l2"] <= 1e-2, h
+        # With three keys dQ and dK are small differences of near-equal terms:
+        # allow the derived delta_lp bound on top of relative 1e-2.
+        for name, r, b in zip(("dq", "dk"), g_ref[:2], delta_error_bound(f, scale, causal)):
+            err = np.linalg.norm(got[name][h] - r)
+            assert err <= 1e-2 * np.linalg.norm(r) + np.linalg.norm(b), (h, name)
