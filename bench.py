@@ -424,7 +424,7 @@ def run_deviation(args):
     For O, LSE, dQ, dK, dV: the tiled GPU kernel, the tiled GPU kernel with
     the stabilised normaliser (beta = 2; on the exact-tie workload also beta =
     1.05, 1.5 and 4), and the naive BF16 attention, each against the FP64
-    definition.  Also delta = rowsum(dO o O) formed from the
+    definition; for O and LSE also the INT8-input forward.  Also delta = rowsum(dO o O) formed from the
     GPU's BF16 O (delta_lp, what the backward uses) against delta from the
     exact O ("Why Low-Precision Transformer Training Fails", Figure 3).
     """
@@ -473,6 +473,14 @@ def run_deviation(args):
             rep[tag]["delta"] = deviation(oracle.delta(f["do"], o_lp), oracle.delta(f["do"], o_ref))
         for k in ref:
             rep["naive_bf16"][k] = deviation(naive[k], ref[k])
+        # INT8-input forward (per-token INT8 Q and K, BF16 V): O and LSE only
+        q8, qs = attn.attn_quantize_int8(t["q"])
+        k8, ks = attn.attn_quantize_int8(t["k"])
+        o8, l8 = attn.attn_fwd_int8(q8, qs, k8, ks, t["v"], scale=w.scale, causal=w.causal)
+        attn.attn_check_status()
+        rep["int8_gpu"] = {
+            "o": deviation(o8.reshape(w.B * w.H, w.N, w.d)[head].float().cpu().numpy(), ref["o"]),
+            "lse": deviation(l8.reshape(w.B * w.H, w.N)[head].cpu().numpy(), ref["lse"])}
         print(json.dumps(rep), flush=True)
     return 0
 
