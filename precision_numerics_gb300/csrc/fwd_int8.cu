@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256) quantize_int8_kernel(const uint16_t* __re
 
 // ---------------------------------------------------------------- attention
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kI8Threads)
+__global__ void __launch_bounds__(kI8Threads, 3)  // 3 CTAs per SM: 168 registers
     fwd_int8_kernel(const int8_t* __restrict__ q8, const float* __restrict__ qs,
                     const int8_t* __restrict__ k8, const float* __restrict__ ks,
                     const uint16_t* __restrict__ v, uint16_t* __restrict__ o,
