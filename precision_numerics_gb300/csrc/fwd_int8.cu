@@ -89,33 +89,58 @@ __device__ __forceinline__ void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, ui
 // ----------------------------------------------------------------- quantize
 // One warp per row of d values: FP32 max|x| by shuffles, s = max / 127,
 // codes rint(x / s) clamped to +-127 (rint: half to even), zero row -> 0.
+constexpr int kQuantRowsPerWarp = 4;  // rows loaded up front per warp (memory-level parallelism)
+
 template <int D>
 __global__ void __launch_bounds__(256) quantize_int8_kernel(const uint16_t* __restrict__ x,
                                                             int8_t* __restrict__ codes,
                                                             float* __restrict__ scales,
                                                             long long rows) {
-  constexpr int kPer = D / 32;  // values per lane
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  constexpr int kPer = D / 32;  // values per lane: 4 (one 8-byte load) or 2 (one 4-byte load)
+  constexpr int R = kQuantRowsPerWarp;
+  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * R;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint16_t* src = x + row * D + lane * kPer;
-  float v[kPer];
-  float amax = 0.f;
+  uint32_t w[R][kPer / 2];  // BF16 pairs of R rows
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    v[e] = __uint_as_float(static_cast<uint32_t>(src[e]) << 16);
-    amax = fmaxf(amax, fabsf(v[e]));
+  for (int q = 0; q < R; ++q) {
+    const long long row = row0 + q;
+    if (row >= rows) break;
+    if constexpr (kPer == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(x + row * D + lane * kPer);
+      w[q][0] = u.x;
+      w[q][1] = u.y;
+    } else {
+      w[q][0] = *reinterpret_cast<const uint32_t*>(x + row * D + lane * kPer);
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float s = amax / 127.f;
-  int8_t* dst = codes + row * D + lane * kPer;
+  for (int q = 0; q < R; ++q) {
+    const long long row = row0 + q;
+    if (row >= rows) break;  // uniform across the warp
+    float v[kPer];
+    float amax = 0.f;
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const float r = s > 0.f ? rintf(v[e] / s) : 0.f;
-    dst[e] = static_cast<int8_t>(fminf(fmaxf(r, -127.f), 127.f));
+    for (int e = 0; e < kPer; ++e) {
+      v[e] = __uint_as_float(e & 1 ? (w[q][e >> 1] & 0xFFFF0000u) : (w[q][e >> 1] << 16));
+      amax = fmaxf(amax, fabsf(v[e]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = amax / 127.f;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const float r = s > 0.f ? rintf(v[e] / s) : 0.f;
+      const int c = static_cast<int>(fminf(fmaxf(r, -127.f), 127.f));
+      packed |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+    }
+    if constexpr (kPer == 4)
+      *reinterpret_cast<uint32_t*>(codes + row * D + lane * kPer) = packed;
+    else
+      *reinterpret_cast<uint16_t*>(codes + row * D + lane * kPer) = static_cast<uint16_t>(packed);
+    if (lane == 0) scales[row] = s;
   }
-  if (lane == 0) scales[row] = s;
 }
 
 // ---------------------------------------------------------------- attention
@@ -333,7 +358,8 @@ cudaError_t launch_int8_impl(const Problem& p, const int8_t* q8, const float* qs
 cudaError_t launch_quantize_int8(const Problem& p, const void* x, void* codes, float* scales,
                                  cudaStream_t stream) {
   const long long rows = (long long)p.B * p.H * p.N;
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  const long long per_block = 8LL * kQuantRowsPerWarp;
+  const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
   if (p.d == 128)
     quantize_int8_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x),
                                                           static_cast<int8_t*>(codes), scales, rows);
