@@ -179,17 +179,23 @@ __global__ void __launch_bounds__(kThreadsR, 1)
                          const __grid_constant__ CUtensorMap tmDK,  // box 128 rows
                          const __grid_constant__ CUtensorMap tmDV,  // box 128 rows
                          const float* __restrict__ neg_lse2, const float* __restrict__ delta,
-                         float* __restrict__ dqacc, int BH, int N, int Npad, float scale,
-                         float scale_log2) {
+                         float* __restrict__ dqacc, int BH, int N, int Npad, int heads_per_group,
+                         float scale, float scale_log2) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Key tiles with the most query tiles (causal: small j) first.
-  const int j = blockIdx.x / BH;
-  const int bh = blockIdx.x % BH;
+  // CTA order: groups of heads_per_group heads; within a group, key tiles
+  // with the most query tiles (causal: small j) first, then heads.
+  const int n_kt = Npad / kBlockN;
+  const int group = blockIdx.x / (heads_per_group * n_kt);
+  const int in_group = blockIdx.x - group * heads_per_group * n_kt;
+  const int g0 = group * heads_per_group;
+  const int g_size = min(heads_per_group, BH - g0);
+  const int j = in_group / g_size;
+  const int bh = g0 + in_group % g_size;
   const int n_qt = (N + kBM - 1) / kBM;
   const int i_first = CAUSAL ? 2 * j : 0;
   const int nq = max(0, n_qt - i_first);
@@ -611,6 +617,35 @@ cudaError_t dq_convert_impl(const Problem& p, const BwdWorkspace& ws, void* dq,
   return cudaGetLastError();
 }
 
+// Heads per CTA group of the main kernel.  Ordering CTAs by head group keeps
+// the Q / dO tiles, LSE / delta rows and dQ accumulator rows of the heads in
+// flight (about 8 N d bytes per head) inside a 48 MiB share of the L2, so that
+// the key-tile CTAs of a head re-read them from L2 rather than HBM.  Within a
+// group the heaviest key tiles come first; the last group is dispatched last,
+// so it must hold enough work per SM (1.2 x the heaviest CTA) that its
+// heaviest CTAs do not outlast the rest of the launch.  Fewer groups win when
+// the two limits disagree.
+int bwd_heads_per_group(int BH, int N, int d, bool causal) {
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      num_sms = n;
+    else
+      return BH;  // one group: the plain heaviest-first order
+  }
+  const double per_head_bytes = 8.0 * N * d;
+  const int g_l2 = max(1, (int)(48.0 * 1048576.0 / per_head_bytes));
+  const int n_qt = ceil_div(N, r64::kBM), n_kt = n_pad(N) / kBlockN;
+  double tiles_per_head = 0.0;
+  for (int j = 0; j < n_kt; ++j) tiles_per_head += max(0, n_qt - (causal ? 2 * j : 0));
+  const double g_tail = 1.2 * n_qt * num_sms / tiles_per_head;
+  int groups = ceil_div(BH, g_l2);
+  groups = min(groups, max(1, (int)(BH / g_tail)));
+  return ceil_div(BH, groups);
+}
+
 template <int D, bool CAUSAL>
 cudaError_t main_r64_impl(const Problem& p, const CUtensorMap* maps, const BwdWorkspace& ws,
                           cudaStream_t stream) {
@@ -621,9 +656,10 @@ cudaError_t main_r64_impl(const Problem& p, const CUtensorMap* maps, const BwdWo
   const int BH = p.B * p.H;
   const int Npad = n_pad(p.N);
   const int n_kt = Npad / kBlockN;
+  const int hpg = bwd_heads_per_group(BH, p.N, D, CAUSAL);
   kernel<<<dim3(BH * n_kt), dim3(r64::kThreadsR), kSmem, stream>>>(
       maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.neg_lse2, ws.delta, ws.dqacc, BH, p.N,
-      Npad, p.scale, p.scale * 1.4426950408889634f);
+      Npad, hpg, p.scale, p.scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
 
