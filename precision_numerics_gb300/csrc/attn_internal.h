@@ -25,6 +25,26 @@ constexpr int kBlockN = 128;  // key rows per tile
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline int n_pad(int N) { return ceil_div(N, kBlockN) * kBlockN; }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// before the previous kernel in the stream has completed (its set-up then
+// overlaps that kernel's tail), so it must call griddep_wait() before its
+// first global-memory access, in every thread that makes one.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Backward workspace layout (all offsets 256-byte aligned):
 //   neg_lse2 FP32 [B*H][Npad] -(LSE * log2(e)); -inf for padded rows
 //   delta FP32 [B*H][Npad]    rowsum(dO o O); 0 for padded rows

@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(256)
                           int blocks_per_head) {
   constexpr int kGroup = D / 8;
   constexpr int kRows = 256 / kGroup;
+  griddep_launch_dependents();
+  griddep_wait();  // O and LSE come from the forward just before
   // One-dimensional grid (B*H may exceed the 65535 limit of gridDim.y).
   const int bh = (int)(blockIdx.x / (unsigned)blocks_per_head);
   const int row = (int)(blockIdx.x % (unsigned)blocks_per_head) * kRows + threadIdx.x / kGroup;
@@ -86,6 +88,8 @@ template <int D>
 __global__ void __launch_bounds__(256)
     bwd_dq_convert_kernel(const float4* __restrict__ dqacc, uint4* __restrict__ dq, int N,
                           int Npad, float scale, int total_units) {
+  griddep_launch_dependents();
+  griddep_wait();  // the accumulator is complete once the main kernel is
   const int u = blockIdx.x * blockDim.x + threadIdx.x;  // one unit = 8 columns of one row
   if (u >= total_units) return;
   constexpr int kUnitsPerRow = D / 8;
@@ -218,9 +222,10 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  // The next kernel in the stream may be scheduled once every CTA is running.
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     *s_abort = (smem_u32(smem) & 1023u) != 0;
-    if (*s_abort) set_fail(ATTN_ERR_INVALID_ARG);
     mbar_init(bar_kv, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_qfull[s], 1);
@@ -250,6 +255,10 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool abort_all = *s_abort != 0 || nq == 0;
+  // Set-up above touches no global memory; from here on the preprocess
+  // kernel's results must be complete and visible.
+  griddep_wait();
+  if (threadIdx.x == 0 && *s_abort != 0) set_fail(ATTN_ERR_INVALID_ARG);
 
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
@@ -600,10 +609,9 @@ cudaError_t preprocess_impl(const Problem& p, const void* o, const void* dout, c
   const int Npad = n_pad(p.N);
   const int per_head = ceil_div(Npad, kRows);
   const unsigned blocks = (unsigned)per_head * (unsigned)(p.B * p.H);
-  bwd_preprocess_kernel<D><<<blocks, 256, 0, stream>>>(
-      static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, ws.neg_lse2, ws.delta,
-      reinterpret_cast<float4*>(ws.dqacc), p.N, Npad, per_head);
-  return cudaGetLastError();
+  return launch_pdl(bwd_preprocess_kernel<D>, dim3(blocks), dim3(256), 0, stream,
+                    static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, ws.neg_lse2,
+                    ws.delta, reinterpret_cast<float4*>(ws.dqacc), p.N, Npad, per_head);
 }
 
 template <int D>
@@ -611,10 +619,9 @@ cudaError_t dq_convert_impl(const Problem& p, const BwdWorkspace& ws, void* dq,
                             cudaStream_t stream) {
   const long long units = (long long)p.B * p.H * p.N * (D / 8);
   const int blocks = (int)((units + 255) / 256);
-  bwd_dq_convert_kernel<D><<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws.dqacc),
-                                                       static_cast<uint4*>(dq), p.N, n_pad(p.N),
-                                                       p.scale, (int)units);
-  return cudaGetLastError();
+  return launch_pdl(bwd_dq_convert_kernel<D>, dim3(blocks), dim3(256), 0, stream,
+                    reinterpret_cast<const float4*>(ws.dqacc), static_cast<uint4*>(dq), p.N,
+                    n_pad(p.N), p.scale, (int)units);
 }
 
 // Heads per CTA group of the main kernel.  Ordering CTAs by head group keeps
@@ -657,10 +664,10 @@ cudaError_t main_r64_impl(const Problem& p, const CUtensorMap* maps, const BwdWo
   const int Npad = n_pad(p.N);
   const int n_kt = Npad / kBlockN;
   const int hpg = bwd_heads_per_group(BH, p.N, D, CAUSAL);
-  kernel<<<dim3(BH * n_kt), dim3(r64::kThreadsR), kSmem, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], ws.neg_lse2, ws.delta, ws.dqacc, BH, p.N,
-      Npad, hpg, p.scale, p.scale * 1.4426950408889634f);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(BH * n_kt), dim3(r64::kThreadsR), kSmem, stream, maps[0], maps[1],
+                    maps[2], maps[3], maps[4], maps[5], static_cast<const float*>(ws.neg_lse2),
+                    static_cast<const float*>(ws.delta), ws.dqacc, BH, p.N, Npad, hpg, p.scale,
+                    p.scale * 1.4426950408889634f);
 }
 
 }  // namespace

@@ -114,9 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n1 = kv_tiles_for(q0 + kBlockM, N, CAUSAL);
   const int nmax = max(n0, n1);
 
+  // The next kernel in the stream may be scheduled once every CTA is running.
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     *s_abort = (smem_u32(smem) & 1023u) != 0;
-    if (*s_abort) set_fail(ATTN_ERR_INVALID_ARG);
     mbar_init(bar_q, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bar_kfull[s], 1);
@@ -143,6 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool abort_all = *s_abort != 0;
+  // Set-up above touches no global memory; from here on the previous kernel's
+  // results must be complete and visible.
+  griddep_wait();
+  if (threadIdx.x == 0 && abort_all) set_fail(ATTN_ERR_INVALID_ARG);
 
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sK = smem + C::kOffK;
@@ -488,10 +493,8 @@ cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUten
   const int BH = p.B * p.H;
   const int num_qt = ceil_div(p.N, 2 * kBlockM);
   const float scale_log2 = p.scale * 1.4426950408889634f;
-  kernel<<<dim3(BH * num_qt), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, mo, lse, BH, p.N,
-                                                                       num_qt, p.scale, scale_log2,
-                                                                       beta);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(BH * num_qt), dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mo,
+                    lse, BH, p.N, num_qt, p.scale, scale_log2, beta);
 }
 
 }  // namespace

@@ -104,6 +104,24 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+// A kernel launched with programmatic stream serialization (launch_pdl) may
+// be scheduled while the previous kernel in the stream is still running.
+// griddep_wait() returns once that kernel has completed and its memory
+// operations are visible to the calling thread, so every thread calls it
+// before its first global-memory access.  griddep_launch_dependents() lets
+// the next such kernel be scheduled once every CTA of this grid has issued
+// it (or exited).  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) and plain bulk copies
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
