@@ -2,6 +2,7 @@
 // the BF16 tensor-core kernels or the FP32 reference-mode kernels, and the
 // device status words behind attn_check_status().
 #include <math.h>
+#include <atomic>
 #include <mutex>
 #include <stdarg.h>
 #include <stdio.h>
@@ -118,6 +119,22 @@ EncodeTiledFn encode_tiled_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   return fn;
+}
+
+int device_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 0;
+  if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 bool make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {

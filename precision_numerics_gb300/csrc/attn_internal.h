@@ -94,6 +94,9 @@ cudaError_t read_and_clear_status_misc(unsigned int* out, cudaStream_t stream);
 // Record the detail text returned by attn_last_error() on this thread.
 void set_last_error(const char* msg);
 
+// Number of SMs of the current device (cached per device); 0 if the query fails.
+int device_sm_count();
+
 // Driver entry point for cuTensorMapEncodeTiled (resolved once, no -lcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

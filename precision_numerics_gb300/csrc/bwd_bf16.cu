@@ -633,15 +633,8 @@ cudaError_t dq_convert_impl(const Problem& p, const BwdWorkspace& ws, void* dq,
 // heaviest CTAs do not outlast the rest of the launch.  Fewer groups win when
 // the two limits disagree.
 int bwd_heads_per_group(int BH, int N, int d, bool causal) {
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      num_sms = n;
-    else
-      return BH;  // one group: the plain heaviest-first order
-  }
+  const int num_sms = device_sm_count();
+  if (num_sms <= 0) return BH;  // one group: the plain heaviest-first order
   const double per_head_bytes = 8.0 * N * d;
   const int g_l2 = max(1, (int)(48.0 * 1048576.0 / per_head_bytes));
   const int n_qt = ceil_div(N, r64::kBM), n_kt = n_pad(N) / kBlockN;

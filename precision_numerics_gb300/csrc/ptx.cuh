@@ -159,6 +159,12 @@ __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Wait until every committed bulk store has finished reading its shared-memory
+// source (the global writes may still be in flight).
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Plain (untiled) bulk copy global -> shared; 16-byte aligned, size % 16 == 0.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {
