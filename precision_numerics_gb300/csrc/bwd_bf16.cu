@@ -19,10 +19,14 @@
 //                   from the tile holding query j * 128 on) with Q_i, dO_i,
 //                   LSE_i, delta_i streamed by TMA.  Five tcgen05 MMAs per
 //                   tile (described at r64 below); dQ_i is added into the FP32
-//                   accumulator with red.global.add.f32.  Both head dims (64
-//                   and 128) use this kernel.
+//                   accumulator with red.global.add.f32.  d = 128 launches
+//                   one CTA per (b, h, j); d = 64 runs the same pipeline in
+//                   persistent CTAs (bwd_main_persistent_kernel), one per SM,
+//                   each walking a list of (b, h, j) items.
 //   3. dq_convert   dQ = bf16(scale * accumulator).  Memory-bound.
 #include <math.h>
+
+#include <algorithm>
 
 #include <type_traits>
 
@@ -600,6 +604,546 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// 2'. main kernel, persistent variant (used for d = 64)
+// ---------------------------------------------------------------------------
+// The pipeline above, in CTAs that stay resident: each CTA walks a static
+// list of (b, h, j) items (heaviest first, dealt in snake order), with the
+// barrier phases counted across items.  An item's first Q / dO tile loads
+// while the previous item finishes; its K_j / V_j load once the previous
+// item's products have completed; its first S^T and dP^T products are issued
+// while the compute warps still write the previous item's dV and dK, which
+// warp 3 stores with TMA from two staging slots.
+// Persistent variant (d = 64): the shared-memory layout of Cfg plus one
+// staging slot each for dV and dK (a 64-column chunk, 128 rows x 128 bytes):
+// the Q / dO rings already hold the next item's tiles during an epilogue.
+// kv_full, q_full[3], q_empty[3], s_full[2], p_ready[2], dp_full, ds_ready,
+// dq_full, dq_free, dq_done[2], item_done, mma_final, epi_full[2], epi_free[2]
+constexpr int kNumBarsP = 1 + 3 + 3 + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 1 + 1 + 2 + 2;
+template <int D>
+struct PCfg : Cfg<D> {
+  using B = Cfg<D>;
+  static constexpr int kOffStage = B::kOffDS + 2 * kDSBytes;
+  static constexpr int kOffLse = kOffStage + 2 * kKVChunk;
+  static constexpr int kOffDelta = kOffLse + kStages * kBM * 4;
+  static constexpr int kOffBar = kOffDelta + kStages * kBM * 4;
+  static constexpr int kSmemBytes = kOffBar + kNumBarsP * 8 + 16;
+};
+
+// Work item L of the main kernel: head bh, key tile j, and its query tiles.
+// Items are numbered by groups of hpg heads; within a group, key tiles with
+// the most query tiles (causal: small j) first, then heads.
+struct BwdItem {
+  int bh, j, i_first, nq;
+};
+__device__ __forceinline__ BwdItem bwd_item(int L, int BH, int n_kt, int n_qt, int hpg,
+                                            bool causal) {
+  const int group = L / (hpg * n_kt);
+  const int in_group = L - group * hpg * n_kt;
+  const int g0 = group * hpg;
+  const int g_size = min(hpg, BH - g0);
+  BwdItem it;
+  it.j = in_group / g_size;
+  it.bh = g0 + in_group % g_size;
+  it.i_first = causal ? 2 * it.j : 0;
+  it.nq = max(0, n_qt - it.i_first);
+  return it;
+}
+
+// Item of round r for this CTA in snake order, or -1 once the list is done
+// (every later round is past the end as well).
+__device__ __forceinline__ int item_of(int r, int total) {
+  const long long G = gridDim.x;
+  const long long c = (r & 1) ? (G - 1 - (long long)blockIdx.x) : (long long)blockIdx.x;
+  const long long idx = (long long)r * G + c;
+  return idx < total ? (int)idx : -1;
+}
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsR, 1)
+    bwd_main_persistent_kernel(const __grid_constant__ CUtensorMap tmQ,   // box 64 rows
+                         const __grid_constant__ CUtensorMap tmK,   // box 128 rows
+                         const __grid_constant__ CUtensorMap tmV,   // box 128 rows
+                         const __grid_constant__ CUtensorMap tmDO,  // box 64 rows
+                         const __grid_constant__ CUtensorMap tmDK,  // box 128 rows
+                         const __grid_constant__ CUtensorMap tmDV,  // box 128 rows
+                         const float* __restrict__ neg_lse2, const float* __restrict__ delta,
+                         float* __restrict__ dqacc, int BH, int N, int Npad, int heads_per_group,
+                         float scale, float scale_log2) {
+  using C = PCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_kt = Npad / kBlockN;
+  const int n_qt = (N + kBM - 1) / kBM;
+  const int total = BH * n_kt;
+  auto item = [&](int L) { return bwd_item(L, BH, n_kt, n_qt, heads_per_group, CAUSAL); };
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* bar_kv = bars + 0;
+  uint64_t* bar_qfull = bars + 1;    // [3]
+  uint64_t* bar_qempty = bars + 4;   // [3]
+  uint64_t* bar_sfull = bars + 7;    // [2]
+  uint64_t* bar_pready = bars + 9;   // [2]
+  uint64_t* bar_dpfull = bars + 11;
+  uint64_t* bar_dsready = bars + 12;
+  uint64_t* bar_dqfull = bars + 13;
+  uint64_t* bar_dqfree = bars + 14;
+  uint64_t* bar_dqdone = bars + 15;  // [2]
+  uint64_t* bar_itemdone = bars + 17;  // every product of an item has completed
+  uint64_t* bar_final = bars + 18;
+  uint64_t* bar_epifull = bars + 19;   // [2] a staged dV / dK chunk is complete
+  uint64_t* bar_epifree = bars + 21;   // [2] its TMA store has read the staging slot
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarsP);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  // The next kernel in the stream may be scheduled once every CTA is running.
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    *s_abort = (smem_u32(smem) & 1023u) != 0;
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_qfull[s], 1);
+      mbar_init(&bar_qempty[s], 1 + 8);  // MMA commit + one arrive per compute warp
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_sfull[b], 1);
+      mbar_init(&bar_pready[b], 256);
+      mbar_init(&bar_dqdone[b], 1);
+      mbar_init(&bar_epifull[b], 128);
+      mbar_init(&bar_epifree[b], 1);
+    }
+    mbar_init(bar_dpfull, 1);
+    mbar_init(bar_dsready, 256);
+    mbar_init(bar_dqfull, 1);
+    mbar_init(bar_dqfree, 128);
+    mbar_init(bar_itemdone, 1);
+    mbar_init(bar_final, 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool abort_all = *s_abort != 0;
+  // Set-up above touches no global memory; from here on the preprocess
+  // kernel's results must be complete and visible.
+  griddep_wait();
+  if (threadIdx.x == 0 && abort_all) set_fail(ATTN_ERR_INVALID_ARG);
+
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sDO = smem + C::kOffDO;
+  uint8_t* sDS = smem + C::kOffDS;
+  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* sDelta = reinterpret_cast<float*>(smem + C::kOffDelta);
+
+  // Barrier phases run on across items.  Every role numbers the 64-row query
+  // tiles it has handled in this CTA (T); the Q / dO ring slot is T % 3, the
+  // S^T buffer T % 2, and the per-tile barriers complete once per T.  Items
+  // with no query tile (none occur for the shapes accepted) are skipped by
+  // every role alike.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG0));
+    if (warp == 0 && lane == 0 && !abort_all) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      bool ok = true;
+      int T = 0, items = 0;
+      auto load_q = [&](int tile, int bh) -> bool {
+        const int st = T % kStages, use = T / kStages;
+        if (use > 0 && !mbar_wait(&bar_qempty[st], (use - 1) & 1)) return false;
+        mbar_arrive_expect_tx(&bar_qfull[st], 2 * C::kQBytes + 2 * kBM * 4);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(sQ + st * C::kQBytes + c * kQChunk, &tmQ, &bar_qfull[st], c * 64, tile * kBM,
+                      bh);
+          tma_load_3d(sDO + st * C::kQBytes + c * kQChunk, &tmDO, &bar_qfull[st], c * 64,
+                      tile * kBM, bh);
+        }
+        const size_t prow = (size_t)bh * Npad + (size_t)tile * kBM;
+        bulk_load(sLse + st * kBM, neg_lse2 + prow, kBM * 4, &bar_qfull[st]);
+        bulk_load(sDelta + st * kBM, delta + prow, kBM * 4, &bar_qfull[st]);
+        ++T;
+        return true;
+      };
+      for (int rr = 0; ok; ++rr) {
+        const int L = item_of(rr, total);
+        if (L < 0) break;
+        const BwdItem it = item(L);
+        if (it.nq == 0) continue;
+        // The item's first Q / dO tile, then K_j and V_j once the previous
+        // item's products (the last to read K and V) have completed.
+        if (!load_q(it.i_first, it.bh)) { ok = false; break; }
+        if (items > 0 && !mbar_wait(bar_itemdone, (items - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar_kv, 2 * C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(sK + c * kKVChunk, &tmK, bar_kv, c * 64, it.j * kBlockN, it.bh);
+          tma_load_3d(sV + c * kKVChunk, &tmV, bar_kv, c * 64, it.j * kBlockN, it.bh);
+        }
+        ++items;
+        for (int q = 1; q < it.nq; ++q)
+          if (!load_q(it.i_first + q, it.bh)) { ok = false; break; }
+      }
+      if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      if (items > 0) mbar_wait(bar_kv, (items - 1) & 1);
+      for (int x = max(0, T - kStages); x < T; ++x)
+        mbar_wait(&bar_qfull[x % kStages], (x / kStages) & 1);
+    } else if (warp == 1 && !abort_all) {
+      // ------------------------------------------------------------ MMA issuer
+      // Whole warp, warp-uniform operands; elect.sync picks the issuing lane.
+      constexpr uint32_t idesc_s = idesc_bf16(128, kBM, false, false);  // K-major A and B
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // TMEM A, MN-major B
+      constexpr uint32_t idesc_dq = idesc_bf16(D, kBM, true, true);     // MN-major A and B
+      const uint64_t kK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t kV = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t kQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t kDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t mQ = sdesc_sw128(smem_u32(sQ), kQChunk, 1024);
+      const uint64_t mDO = sdesc_sw128(smem_u32(sDO), kQChunk, 1024);
+      const uint64_t mK = sdesc_sw128(smem_u32(sK), kKVChunk, 1024);
+      const uint64_t mDS = sdesc_sw128(smem_u32(sDS), kDSBytes, 1024);
+      // S^T or dP^T (into column d_col) = X_j Y_i^T over the d head dims.
+      auto issue_xy = [&](uint32_t d_col, uint64_t dX, uint64_t dY, uint32_t y_off) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t cx = (kk >> 2) * kKVChunk + (kk & 3) * 32;
+          const uint32_t cy = (kk >> 2) * kQChunk + (kk & 3) * 32;
+          mma_ss_elect(tmem + d_col, sdesc_add(dX, cx), sdesc_add(dY, y_off + cy), idesc_s,
+                       kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+      int T0 = 0, items = 0;
+      for (int rr = 0; ok; ++rr) {
+        const int L = item_of(rr, total);
+        if (L < 0) break;
+        const BwdItem it = item(L);
+        if (it.nq == 0) continue;
+        // Prologue: S^T(T0), dP^T(T0), S^T(T0+1).  The S buffers, the dP region
+        // and (below) dV / dK are free: the products of the previous item that
+        // read them were issued earlier on this thread, and the compute warps
+        // finished reading dV / dK before producing this item's first P and dS.
+        ok = warp_wait(bar_kv, items & 1);
+        if (ok) ok = warp_wait(&bar_qfull[T0 % kStages], (T0 / kStages) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_xy(C::kColS + (T0 & 1) * kBM, kK, kQ, (T0 % kStages) * C::kQBytes);
+        mma_commit_elect(&bar_sfull[T0 & 1]);
+        issue_xy(C::kColDP, kV, kDO, (T0 % kStages) * C::kQBytes);
+        mma_commit_elect(bar_dpfull);
+        if (it.nq > 1) {
+          const int T1 = T0 + 1;
+          ok = warp_wait(&bar_qfull[T1 % kStages], (T1 / kStages) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_xy(C::kColS + (T1 & 1) * kBM, kK, kQ, (T1 % kStages) * C::kQBytes);
+          mma_commit_elect(&bar_sfull[T1 & 1]);
+        }
+        for (int q = 0; q < it.nq && ok; ++q) {
+          const int T = T0 + q;
+          const int st = T % kStages, b = T & 1;
+          const uint32_t so = st * C::kQBytes;
+          // dV += P^T dO_i
+          if (!warp_wait(&bar_pready[b], (T >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBM / 16; ++kk)
+            mma_ts_elect(tmem + C::kColDV, tmem + C::kColS + b * kBM + packed_col(kk),
+                         sdesc_add(mDO, so + kk * 2048), idesc_acc, (q > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q_i
+          if (!warp_wait(bar_dsready, T & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBM / 16; ++kk)
+            mma_ts_elect(tmem + C::kColDK, tmem + C::kColDP + packed_col(kk),
+                         sdesc_add(mQ, so + kk * 2048), idesc_acc, (q > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_elect(&bar_qempty[st]);
+          // dP^T(T+1): the dP region is free (dK(T) above read dS^T from it).
+          if (q + 1 < it.nq) {
+            issue_xy(C::kColDP, kV, kDO, ((T + 1) % kStages) * C::kQBytes);
+            mma_commit_elect(bar_dpfull);
+          }
+          // dQ^T(T) = K_j^T dS^T(T)
+          if (T > 0 && !warp_wait(bar_dqfree, (T - 1) & 1)) { ok = false; break; }
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk)
+            mma_ss_elect(tmem + C::kColDQ, sdesc_add(mK, kk * 2048),
+                         sdesc_add(mDS, b * kDSBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
+          mma_commit_elect(bar_dqfull);
+          mma_commit_elect(&bar_dqdone[b]);
+          // S^T(T+2) into buffer b (P^T(T) was read by dV(T) above).
+          if (q + 2 < it.nq) {
+            const int T2 = T + 2;
+            if (!warp_wait(&bar_qfull[T2 % kStages], (T2 / kStages) & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_xy(C::kColS + b * kBM, kK, kQ, (T2 % kStages) * C::kQBytes);
+            mma_commit_elect(&bar_sfull[b]);
+          }
+        }
+        if (!ok) break;
+        // dV, dK complete; K and V may be replaced.
+        mma_commit_elect(bar_itemdone);
+        T0 += it.nq;
+        ++items;
+      }
+      if (!ok && lane == 0) set_fail(ATTN_ERR_TIMEOUT);
+      mma_commit_elect(bar_final);
+      mbar_wait(bar_final, 0);
+    } else if (warp == 3 && lane == 0 && !abort_all) {
+      // ---------------------------------------------------- dV / dK stores
+      // One TMA store per staged 64-column chunk; the staging slot is handed
+      // back once the store has read it.
+      bool ok = true;
+      int es[2] = {0, 0};
+      for (int rr = 0; ok; ++rr) {
+        const int L = item_of(rr, total);
+        if (L < 0) break;
+        const BwdItem it = item(L);
+        if (it.nq == 0) continue;
+        for (int c = 0; c < C::kChunks && ok; ++c)
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(&bar_epifull[h], es[h] & 1)) { ok = false; break; }
+            tma_store_3d(h == 0 ? &tmDV : &tmDK, smem + C::kOffStage + h * kKVChunk, c * 64,
+                         it.j * kBlockN, it.bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(&bar_epifree[h]);
+            ++es[h];
+          }
+      }
+      if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+      // The output stores complete before this CTA ends.
+      bulk_wait_group0();
+    }
+    __syncwarp();
+  } else if (warp >= 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDrain));
+    // ------------------------------------------------------------ dQ drain
+    // dQ^T(T), all 64 query columns: each thread adds one head dim of every
+    // query row; a warp's reductions of one column cover contiguous bytes.
+    // d = 128 (M = 128): head dim m is TMEM lane m, 32 per warp.  d = 64
+    // (M = 64): head dim m is lane (m / 16) * 32 + m % 16, so lanes 0-15 of
+    // each warp hold 16 head dims and lanes 16-31 hold nothing of dQ^T.
+    const int dim = D == 128 ? (warp & 3) * 32 + lane : (warp & 3) * 16 + (lane & 15);
+    const bool holds_dim = D == 128 || lane < 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tDQ = tmem + lane_off + C::kColDQ;
+    bool ok = !abort_all;
+    int T = 0;
+    for (int rr = 0; ok; ++rr) {
+      const int L = item_of(rr, total);
+      if (L < 0) break;
+      const BwdItem it = item(L);
+      for (int q = 0; q < it.nq && ok; ++q, ++T) {
+        ok = warp_wait(bar_dqfull, T & 1);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t acc[2][32];
+        tmem_ld32(tDQ, acc[0]);
+        tmem_ld32(tDQ + 32, acc[1]);
+        tmem_wait_ld();
+        reg_fence(acc[0]);
+        reg_fence(acc[1]);
+        tc_fence_before();
+        mbar_arrive(bar_dqfree);
+        float* dst = dqacc + ((size_t)it.bh * Npad + (size_t)(it.i_first + q) * kBM) * D + dim;
+        if (holds_dim) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + (size_t)c * D),
+                         "f"(__uint_as_float(acc[c >> 5][c & 31]))
+                         : "memory");
+        }
+      }
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
+    // ------------------------------------------- P and dS (two warpgroups)
+    // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) owns query columns
+    // [32h, 32h+32) of every 64-row tile: it computes those columns of P^T
+    // and dS^T (thread = key row = TMEM lane).  After an item it writes dV
+    // (h = 0) or scale * dK (h = 1).
+    const int h = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tDP = tmem + lane_off + C::kColDP;
+    const uint32_t dsBase0 = smem_u32(sDS);
+    const uint32_t aStage = smem_u32(smem + C::kOffStage + h * kKVChunk);
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+    bool ok = !abort_all;
+    int T = 0, items = 0, es = 0;
+    for (int rr = 0; ok; ++rr) {
+      const int L = item_of(rr, total);
+      if (L < 0) break;
+      const BwdItem itm = item(L);
+      if (itm.nq == 0) continue;
+      const int j = itm.j;
+      const int kv = j * kBlockN + r;
+      const bool key_valid = kv < N;
+      for (int q = 0; q < itm.nq && ok; ++q, ++T) {
+        const int st = T % kStages, b = T & 1;
+        const int i = itm.i_first + q;
+        const uint32_t tS = tmem + lane_off + C::kColS + b * kBM;
+        ok = warp_wait(&bar_qfull[st], (T / kStages) & 1);
+        if (!ok) break;
+        ok = warp_wait(&bar_sfull[b], (T >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t p[32];
+        tmem_ld32(tS + h * 32, p);
+        tmem_wait_ld();
+        reg_fence(p);
+        const float* L2 = sLse + st * kBM + h * 32;
+        // P = exp2(c s - LSE log2 e), the argument of each column pair in one
+        // packed FP32 fma (bit-identical to two scalar fmas).  Local column c is
+        // query i*64 + 32h + c.  Causal: it sees this key only when c >= vis_to;
+        // padded keys see nothing.  Only tiles that cross the diagonal or hold
+        // padded keys take the masked loop.  Padded queries have
+        // -LSE log2(e) = -inf, so their P is 0 already.
+        const int vis_to = CAUSAL ? kv - i * kBM - h * 32 : 0;
+        const bool need_mask =
+            (CAUSAL && i * kBM < (j + 1) * kBlockN) || (j + 1) * kBlockN > N;
+        auto p_block = [&](auto masked) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(L2 + c);
+            const uint64_t l2[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              const int cc = c + e;
+              float x0, x1;
+              f2_unpack(fma2(f2_pack(__uint_as_float(p[cc]), __uint_as_float(p[cc + 1])), c2,
+                             l2[e >> 1]),
+                        x0, x1);
+              float p0 = ex2(x0), p1 = ex2(x1);
+              if (decltype(masked)::value) {
+                if (!key_valid || cc < vis_to) p0 = 0.f;
+                if (!key_valid || cc + 1 < vis_to) p1 = 0.f;
+              }
+              p[cc] = __float_as_uint(p0);
+              p[cc + 1] = __float_as_uint(p1);
+            }
+          }
+        };
+        if (need_mask) {
+          p_block(std::true_type{});
+        } else {
+          p_block(std::false_type{});
+        }
+        {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1]));
+          tmem_st16(tS + h * 32, pk);  // inside this warpgroup's own S columns
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_pready[b]);
+
+        ok = warp_wait(bar_dpfull, T & 1);
+        if (!ok) break;
+        // dS^T buffer b is free once dQ^T(T-2), which read it, has completed.
+        if (T >= 2) {
+          ok = warp_wait(&bar_dqdone[b], ((T >> 1) - 1) & 1);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const float* Dl = sDelta + st * kBM + h * 32;
+        {
+          uint32_t dp[32];
+          tmem_ld32(tDP + h * 32, dp);
+          tmem_wait_ld();
+          reg_fence(dp);
+          uint32_t pk[16];
+          // dS = P o (dP - delta): dP - delta as fma(delta, -1, dP) (exact
+          // negation, one rounding: the subtraction), then the product, both packed.
+          const uint64_t m1 = f2_pack(-1.f, -1.f);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 d2 = *reinterpret_cast<const float2*>(Dl + 2 * e);
+            const uint64_t diff = fma2(f2_pack(d2.x, d2.y), m1,
+                                       f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])));
+            float ds0, ds1;
+            f2_unpack(mul2(f2_pack(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])), diff),
+                      ds0, ds1);
+            pk[e] = pack_bf16x2(ds0, ds1);
+          }
+          tmem_st16(tDP + h * 32, pk);  // inside this warpgroup's own dP columns
+          // dS^T row r, query columns 32h .. 32h+31: 16-byte units 4h .. 4h+3 of
+          // the row's 128-byte swizzled line (MN-major B operand of dQ^T).
+          const uint32_t dsBase = dsBase0 + b * kDSBytes;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(dsBase + sw128_offset(r, h * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar_dsready);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_qempty[st]);
+      }
+      if (!ok) break;
+      // ------------------------- epilogue: h = 0 writes dV, h = 1 scale * dK
+      // Staged 64 columns at a time in this warpgroup's slot; warp 3 stores
+      // each chunk with TMA.  The next item's first dV / dK products, which
+      // overwrite the accumulators, wait for this warpgroup's next P and dS,
+      // so they cannot run before the accumulators have been read here.
+      ok = warp_wait(bar_itemdone, items & 1);
+      if (!ok) break;
+      ++items;
+      tc_fence_after();
+      const uint32_t tAcc = tmem + lane_off + (h == 0 ? C::kColDV : C::kColDK);
+      const float mul = h == 0 ? 1.f : scale;
+      for (int c = 0; c < C::kChunks && ok; ++c) {
+        // The slot is free once the previous chunk's store has read it.
+        if (es > 0) {
+          ok = warp_wait(&bar_epifree[h], (es - 1) & 1);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t o[32];
+          tmem_ld32(tAcc + c * 64 + hh * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(aStage + sw128_offset(r, hh * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar_epifull[h]);  // warp 3 stores the chunk
+        ++es;
+      }
+    }
+    if (!ok) set_fail(ATTN_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace r64
 
 template <int D>
@@ -663,6 +1207,31 @@ cudaError_t main_r64_impl(const Problem& p, const CUtensorMap* maps, const BwdWo
                     p.scale * 1.4426950408889634f);
 }
 
+// d = 64: persistent CTAs, one per SM, walking the (head, key tile) items in
+// snake order.  The list is ordered heaviest first across all heads (one
+// group): a static schedule over head groups left late heavy items.  On the
+// gpt2 workload this kernel runs the backward main phase in 66 us against 74
+// for one CTA per item; at d = 128 persistence measured slower (311 against
+// 295 us on the llama7b workload), so d = 128 keeps one CTA per item.
+template <int D, bool CAUSAL>
+cudaError_t main_persistent_impl(const Problem& p, const CUtensorMap* maps, const BwdWorkspace& ws,
+                                 cudaStream_t stream) {
+  auto kernel = r64::bwd_main_persistent_kernel<D, CAUSAL>;
+  constexpr int kSmem = r64::PCfg<D>::kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (err != cudaSuccess) return err;
+  const int BH = p.B * p.H;
+  const int Npad = n_pad(p.N);
+  const int n_kt = Npad / kBlockN;
+  const int total = BH * n_kt;
+  const int sms = device_sm_count();
+  const int grid = sms > 0 ? std::min(total, sms) : total;
+  return launch_pdl(kernel, dim3(grid), dim3(r64::kThreadsR), kSmem, stream, maps[0], maps[1],
+                    maps[2], maps[3], maps[4], maps[5], static_cast<const float*>(ws.neg_lse2),
+                    static_cast<const float*>(ws.delta), ws.dqacc, BH, p.N, Npad, BH, p.scale,
+                    p.scale * 1.4426950408889634f);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_preprocess_bf16(const Problem& p, const void* o, const void* dout,
@@ -693,8 +1262,8 @@ cudaError_t launch_bwd_main_bf16(const Problem& p, const void* q, const void* k,
   if (p.d == 128)
     return p.causal ? main_r64_impl<128, true>(p, maps, ws, stream)
                     : main_r64_impl<128, false>(p, maps, ws, stream);
-  return p.causal ? main_r64_impl<64, true>(p, maps, ws, stream)
-                  : main_r64_impl<64, false>(p, maps, ws, stream);
+  return p.causal ? main_persistent_impl<64, true>(p, maps, ws, stream)
+                  : main_persistent_impl<64, false>(p, maps, ws, stream);
 }
 
 cudaError_t read_and_clear_status_bwd(unsigned int* out, cudaStream_t stream) {
