@@ -622,13 +622,23 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 // dq_full, dq_free, dq_done[2], item_done, mma_final, epi_full[2], epi_free[2]
 constexpr int kNumBarsP = 1 + 3 + 3 + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 1 + 1 + 2 + 2;
 template <int D>
-struct PCfg : Cfg<D> {
-  using B = Cfg<D>;
-  static constexpr int kOffStage = B::kOffDS + 2 * kDSBytes;
+struct PCfg {
+  static constexpr int kChunks = D / 64;          // 64-column (128-byte) chunks per row
+  static constexpr int kKVBytes = 128 * D * 2;    // K_j or V_j (128 rows x d)
+  static constexpr int kQBytes = kBM * D * 2;     // Q_i or dO_i (64 rows x d)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKVBytes;
+  static constexpr int kOffQ = kOffV + kKVBytes;
+  static constexpr int kOffDO = kOffQ + kStages * kQBytes;
+  static constexpr int kOffDS = kOffDO + kStages * kQBytes;
+  static constexpr int kOffStage = kOffDS + 2 * kDSBytes;
   static constexpr int kOffLse = kOffStage + 2 * kKVChunk;
   static constexpr int kOffDelta = kOffLse + kStages * kBM * 4;
   static constexpr int kOffBar = kOffDelta + kStages * kBM * 4;
   static constexpr int kSmemBytes = kOffBar + kNumBarsP * 8 + 16;
+  static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128,
+                            kColDQ = 2 * D + 192;
+  static_assert(kColDQ + kBM <= 512, "TMEM columns");
 };
 
 // Work item L of the main kernel: head bh, key tile j, and its query tiles.
