@@ -27,7 +27,7 @@
 //   warp 0      TMA producer (Q once per item; K_j, V_j through a ring)
 //   warp 1      MMA issuer: S_t = Q_t K_j^T, O_t += P_t V_j
 //   warp 2      TMEM allocation owner
-//   warp 3      TMA stores of the staged output
+//   warp 3      TMA stores of the staged output (d = 128)
 //   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1; each
 //               thread owns one query row (one TMEM lane), so row max and
 //               row sum need no cross-thread reduction.  They also stage
@@ -68,9 +68,13 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  // Output staging: one 64-column chunk (128 rows x 128 bytes) per query tile.
+  // Output: at d = 128 staged one 64-column chunk (128 rows x 128 bytes) per
+  // query tile and written by TMA; at d = 64 each thread's row is one 128-byte
+  // line, written straight from registers (measured ~5% faster there; at
+  // d = 128 the direct stores were ~1.5% slower).
+  static constexpr bool kStagedOut = (D == 128);
   static constexpr int kOffStage = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffStage + 2 * kChunkBytes;
+  static constexpr int kOffBar = kOffStage + (kStagedOut ? 2 * kChunkBytes : 0);
   // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
   // p_full[2], o_done[2], mma_final, alpha[2][4] (one per tile and softmax
   // warp), epi_full[2], epi_free[2]
@@ -122,7 +126,7 @@ template <int D, bool CAUSAL, bool STABLE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    float* __restrict__ lse, int BH, int N, int num_qt, float scale,
+                    uint16_t* __restrict__ out, float* __restrict__ lse, int BH, int N, int num_qt, float scale,
                     float scale_log2, float beta) {
   using C = FwdCfg<D>;
   static_assert(kRegsWG0 + kRegsCorr + 2 * kRegsSoftmax <= 512, "setmaxnreg split exceeds the launch pool");
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every MMA this warp issued completes before TMEM is released.
       mma_commit_elect(bar_final);
       mbar_wait(bar_final, 0);
-    } else if (warp == 3 && lane == 0 && !abort_all) {
+    } else if (C::kStagedOut && warp == 3 && lane == 0 && !abort_all) {
       // ------------------------------------------------------------ O stores
       // One TMA store per staged 64-column chunk of O, in the order the
       // softmax warpgroups stage them (tile 0 finishes an item no later than
@@ -542,16 +546,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const uint64_t il2 = f2_pack(inv_l, inv_l);
-      for (int c = 0; c < C::kChunks && ok; ++c) {
-        // The slot is free once the previous chunk's store has read it.
-        if (es > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_epifree[t], (es - 1) & 1));
-          if (!ok) break;
-        }
+      if constexpr (C::kStagedOut) {
+        for (int c = 0; c < C::kChunks && ok; ++c) {
+          // The slot is free once the previous chunk's store has read it.
+          if (es > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_epifree[t], (es - 1) & 1));
+            if (!ok) break;
+          }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 64 + h * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float lo, hi;
+              f2_unpack(mul2(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
+                        lo, hi);
+              pk[i] = pack_bf16x2(lo, hi);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              st_shared_v4(aStage + sw128_offset(r, h * 4 + u), pk[4 * u], pk[4 * u + 1],
+                           pk[4 * u + 2], pk[4 * u + 3]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bar_epifull[t]);  // warp 3 stores the chunk
+          ++es;
+        }
+      } else {
+        uint4* row = reinterpret_cast<uint4*>(out + ((size_t)it.bh * N + qi) * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(tO + c * 64 + h * 32, o);
+          tmem_ld32(tO + c * 32, o);
           tmem_wait_ld();
           reg_fence(o);
           uint32_t pk[16];
@@ -562,14 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       lo, hi);
             pk[i] = pack_bf16x2(lo, hi);
           }
+          if (qi < N) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_shared_v4(aStage + sw128_offset(r, h * 4 + u), pk[4 * u], pk[4 * u + 1],
-                         pk[4 * u + 2], pk[4 * u + 3]);
+            for (int u = 0; u < 4; ++u)
+              row[c * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar_epifull[t]);  // warp 3 stores the chunk
-        ++es;
       }
       if (!ok) break;
       if (qi < N) lse[(size_t)it.bh * N + qi] = m_norm * scale + logf(l_run);
@@ -587,7 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL, bool STABLE>
 cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mo, float* lse, float beta,
+                            const CUtensorMap& mv, const CUtensorMap& mo, void* o, float* lse,
+                            float beta,
                             cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kernel = fwd_bf16_kernel<D, CAUSAL, STABLE>;
@@ -602,8 +631,8 @@ cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUten
   const int sms = device_sm_count();
   const int grid = sms > 0 ? std::min(total, sms) : total;
   const float scale_log2 = p.scale * 1.4426950408889634f;
-  return launch_pdl(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mo, lse,
-                    BH, p.N, num_qt, p.scale, scale_log2, beta);
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mo,
+                    static_cast<uint16_t*>(o), lse, BH, p.N, num_qt, p.scale, scale_log2, beta);
 }
 
 }  // namespace
@@ -618,7 +647,7 @@ cudaError_t launch_fwd_bf16(const Problem& p, const void* q, const void* k, cons
   const bool st = beta > 0.f;  // beta <= 0: the plain kernel
 #define ATTN_FWD_CASE(DD, CC, SS) \
   if (p.d == DD && (p.causal != 0) == CC && st == SS) \
-    return launch_fwd_impl<DD, CC, SS>(p, mq, mk, mv, mo, lse, beta, stream);
+    return launch_fwd_impl<DD, CC, SS>(p, mq, mk, mv, mo, o, lse, beta, stream);
   ATTN_FWD_CASE(128, true, false)
   ATTN_FWD_CASE(128, false, false)
   ATTN_FWD_CASE(64, true, false)
