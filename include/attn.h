@@ -138,6 +138,40 @@ ATTN_API attn_status attn_fwd_int8(const void* q8, const float* q_scale, const v
                                    cudaStream_t stream);
 
 /*
+ * The quantization of attn_quantize_int8 with the codes held in BF16: every
+ * code is an integer in [-127, 127], which BF16 represents exactly, so these
+ * are the same codes in a 2-byte type.  The scales are laid out per head with
+ * the row count padded: scales[(b*H + h) * N_pad + n], N_pad = N rounded up
+ * to a multiple of 128; the padded entries are written as 0.
+ *   x      : [B,H,N,d] BF16, device.
+ *   codes  : [B,H,N,d] BF16, device, written.
+ *   scales : B*H*N_pad FP32, device, written.
+ * d in {64, 128}; all pointers 16-byte aligned.
+ */
+ATTN_API attn_status attn_quantize_int8_as_bf16(const void* x, void* codes, float* scales, int B,
+                                                int H, int N, int d, cudaStream_t stream);
+
+/*
+ * attn_fwd_int8 on codes held in BF16 (attn_quantize_int8_as_bf16): the same
+ * scores S_ij = scale * q_scale[i] * k_scale[j] * (q8_i . k8_j), the integer
+ * dot product exact, evaluated on the BF16 tcgen05 path of attn_fwd -- every
+ * product of two codes (|c| <= 127) and every partial sum over d <= 128
+ * terms (< 2^24) is exact in the FP32 accumulator, whatever the order.  The
+ * row scale is clamped below at 1e-20 (a row of zero codes has zero scores
+ * either way).  Compared with attn_fwd_int8, Q and K take two bytes per code
+ * and the path runs at the speed of the BF16 forward.
+ *   q_codes, k_codes : [B,H,N,d] BF16 holding integer codes, device.
+ *   q_scale, k_scale : B*H*N_pad FP32 (layout of attn_quantize_int8_as_bf16).
+ *   v : [B,H,N,d] BF16.   o : [B,H,N,d] BF16.   lse : [B,H,N] FP32.
+ * d in {64, 128}; all pointers 16-byte aligned, device memory.
+ */
+ATTN_API attn_status attn_fwd_int8_as_bf16(const void* q_codes, const float* q_scale,
+                                           const void* k_codes, const float* k_scale,
+                                           const void* v, void* o, float* lse, int B, int H,
+                                           int N, int d, float scale, int causal,
+                                           cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (0 on invalid
  * arguments).  Layout (internal): -LSE*log2(e) and delta, FP32 [B*H][Npad]
  * each, and the FP32 dQ accumulator [B*H][Npad][d], Npad = N rounded up to

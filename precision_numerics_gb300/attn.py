@@ -24,7 +24,8 @@ ATTN_DTYPE_BF16, ATTN_DTYPE_FP32 = 0, 1
 EXPORTED = ("attn_version", "attn_status_string", "attn_last_error", "attn_fwd",
             "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
             "attn_bwd_dq_convert", "attn_check_status", "attn_selftest_wait_timeout",
-            "attn_bwd_noalloc", "attn_fwd_stable", "attn_quantize_int8", "attn_fwd_int8")
+            "attn_bwd_noalloc", "attn_fwd_stable", "attn_quantize_int8", "attn_fwd_int8",
+            "attn_quantize_int8_as_bf16", "attn_fwd_int8_as_bf16")
 
 
 class AttnError(RuntimeError):
@@ -53,6 +54,8 @@ _SIGNATURES = {
     "attn_fwd_stable": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _f, _i, _vp]),
     "attn_quantize_int8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "attn_fwd_int8": (_i, [_vp] * 7 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "attn_quantize_int8_as_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "attn_fwd_int8_as_bf16": (_i, [_vp] * 7 + [_i, _i, _i, _i, _f, _i, _vp]),
 }
 
 
@@ -204,6 +207,53 @@ def attn_fwd_int8(q8, q_scale, k8, k_scale, v, scale=None, causal=False, o=None,
     _call("attn_fwd_int8", q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
           v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, _default_scale(d, scale),
           int(bool(causal)), _stream(stream))
+    return o, lse
+
+
+def int8_scale_rows(N: int) -> int:
+    """Rows per head of the padded scale layout of the *_as_bf16 INT8 calls (N rounded up to 128)."""
+    return (N + 127) // 128 * 128
+
+
+def _check_padded_scales(name, t, B, H, N):
+    if (tuple(t.shape) != (B, H, int8_scale_rows(N)) or t.dtype != torch.float32
+            or not t.is_contiguous() or not t.is_cuda):
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor [B, H, {int8_scale_rows(N)}]")
+
+
+def attn_quantize_int8_as_bf16(x, codes=None, scales=None, stream=None):
+    """attn_quantize_int8 with the codes held in BF16 and the scales padded to [B, H, N_pad]."""
+    _check_bhnd("x", x, dtype=torch.bfloat16)
+    B, H, N, d = x.shape
+    if codes is None:
+        codes = torch.empty_like(x)
+    if scales is None:
+        scales = torch.empty((B, H, int8_scale_rows(N)), dtype=torch.float32, device=x.device)
+    _check_bhnd("codes", codes, x.shape, torch.bfloat16)
+    _check_padded_scales("scales", scales, B, H, N)
+    _call("attn_quantize_int8_as_bf16", x.data_ptr(), codes.data_ptr(), scales.data_ptr(), B, H, N,
+          d, _stream(stream))
+    return codes, scales
+
+
+def attn_fwd_int8_as_bf16(q_codes, q_scale, k_codes, k_scale, v, scale=None, causal=False, o=None,
+                          lse=None, stream=None):
+    """attn_fwd_int8 on BF16-held codes (attn_quantize_int8_as_bf16), on the tcgen05 path."""
+    _check_bhnd("v", v, dtype=torch.bfloat16)
+    B, H, N, d = v.shape
+    for name, t in (("q_codes", q_codes), ("k_codes", k_codes)):
+        _check_bhnd(name, t, v.shape, torch.bfloat16)
+    _check_padded_scales("q_scale", q_scale, B, H, N)
+    _check_padded_scales("k_scale", k_scale, B, H, N)
+    if o is None:
+        o = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=v.device)
+    _check_bhnd("o", o, v.shape, v.dtype)
+    _check_lse(lse, B, H, N)
+    _call("attn_fwd_int8_as_bf16", q_codes.data_ptr(), q_scale.data_ptr(), k_codes.data_ptr(),
+          k_scale.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+          _default_scale(d, scale), int(bool(causal)), _stream(stream))
     return o, lse
 
 

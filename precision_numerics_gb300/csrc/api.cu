@@ -288,6 +288,33 @@ attn_status attn_fwd_int8(const void* q8, const float* q_scale, const void* k8,
                   "attn_fwd_int8");
 }
 
+attn_status attn_quantize_int8_as_bf16(const void* x, void* codes, float* scales, int B, int H,
+                                       int N, int d, cudaStream_t stream) {
+  Problem p;
+  ATTN_CHECK(check_problem(B, H, N, d, ATTN_DTYPE_BF16, 1.f, false, &p));
+  ATTN_CHECK(check_ptr(x, "x"));
+  ATTN_CHECK(check_ptr(codes, "codes"));
+  ATTN_CHECK(check_ptr(scales, "scales"));
+  return launched(launch_quantize_int8_as_bf16(p, x, codes, scales, stream),
+                  "attn_quantize_int8_as_bf16");
+}
+
+attn_status attn_fwd_int8_as_bf16(const void* q_codes, const float* q_scale, const void* k_codes,
+                                  const float* k_scale, const void* v, void* o, float* lse, int B,
+                                  int H, int N, int d, float scale, int causal,
+                                  cudaStream_t stream) {
+  Problem p;
+  ATTN_CHECK(check_problem(B, H, N, d, ATTN_DTYPE_BF16, scale, true, &p));
+  p.causal = causal != 0;
+  const void* ptrs[7] = {q_codes, q_scale, k_codes, k_scale, v, o, lse};
+  const char* names[7] = {"q_codes", "q_scale", "k_codes", "k_scale", "v", "o", "lse"};
+  for (int i = 0; i < 7; ++i) ATTN_CHECK(check_ptr(ptrs[i], names[i]));
+  if (encode_tiled_fn() == nullptr)
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  return launched(launch_fwd_int8_as_bf16(p, q_codes, q_scale, k_codes, k_scale, v, o, lse, stream),
+                  "attn_fwd_int8_as_bf16");
+}
+
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d, attn_dtype dt) {
   Problem p;
   if (check_problem(B, H, N, d, dt, 1.f, false, &p) != ATTN_OK) return 0;

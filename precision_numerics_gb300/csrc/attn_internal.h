@@ -85,6 +85,13 @@ cudaError_t launch_quantize_int8(const Problem& p, const void* x, void* codes, f
 cudaError_t launch_fwd_int8(const Problem& p, const void* q8, const float* qs, const void* k8,
                             const float* ks, const void* v, void* o, float* lse,
                             cudaStream_t stream);
+// The same on INT8 codes held in BF16, with scales in the padded per-head
+// layout [B*H][n_pad(N)], on the tcgen05 forward kernel.
+cudaError_t launch_quantize_int8_as_bf16(const Problem& p, const void* x, void* codes,
+                                         float* scales, cudaStream_t stream);
+cudaError_t launch_fwd_int8_as_bf16(const Problem& p, const void* qc, const float* qs,
+                                    const void* kc, const float* ks, const void* v, void* o,
+                                    float* lse, cudaStream_t stream);
 
 // Device status words (one per kernel translation unit): read and clear.
 cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream);

@@ -122,12 +122,18 @@ __device__ __forceinline__ Item item_coords(int L, int BH, int N, int num_qt, bo
   return it;
 }
 
-template <int D, bool CAUSAL, bool STABLE>
+// I8: Q and K hold per-token INT8 codes as BF16 values (exact integers), with
+// FP32 row scales qs / ks in the padded layout [B*H][Npad]; the S products
+// are then exact integer dot products (every product |c_q c_k| <= 127^2 and
+// every partial sum over d <= 128 terms stays below 2^24, exact in the FP32
+// accumulator in any order), and the logits are scale * qs_i * ks_j * S_ij.
+template <int D, bool CAUSAL, bool STABLE, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     uint16_t* __restrict__ out, float* __restrict__ lse, int BH, int N, int num_qt, float scale,
-                    float scale_log2, float beta) {
+                    float scale_log2, float beta, const float* __restrict__ qs,
+                    const float* __restrict__ ks, int Npad) {
   using C = FwdCfg<D>;
   static_assert(kRegsWG0 + kRegsCorr + 2 * kRegsSoftmax <= 512, "setmaxnreg split exceeds the launch pool");
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -435,6 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = it.n[t];
       const int q_first = it.q0 + t * kBlockM;
       const int qi = q_first + r;
+      // I8: the row's INT8 scale enters through the exponent factor c_row (a
+      // row of zero codes has zero scores whatever its scale, so the scale is
+      // kept above 1e-20 to keep c_row * -inf at -inf).
+      const float sq = I8 ? fmaxf(qi < N ? qs[(size_t)it.bh * Npad + qi] : 0.f, 1e-20f) : 1.f;
+      const float c_row = I8 ? scale_log2 * sq : scale_log2;
       // m_run: running row max; m_norm: the normaliser the exponentials of the
       // previous tiles used (equal to m_run except in the stabilised variant).
       float m_run = -INFINITY, m_norm = -INFINITY, l_run = 0.f;
@@ -449,6 +460,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence(s[c]);
+        if constexpr (I8) {
+          // S_ij * ks_j: the key scales of this tile (128 FP32, 16-byte aligned in
+          // the padded layout; the entries past N belong to masked keys).
+          const float4* kr = reinterpret_cast<const float4*>(ks + (size_t)it.bh * Npad + j * kBlockN);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 k4 = __ldg(kr + c * 8 + u);
+              float a0, a1, a2, a3;
+              f2_unpack(mul2(f2_pack(__uint_as_float(s[c][4 * u]), __uint_as_float(s[c][4 * u + 1])),
+                             f2_pack(k4.x, k4.y)),
+                        a0, a1);
+              f2_unpack(mul2(f2_pack(__uint_as_float(s[c][4 * u + 2]), __uint_as_float(s[c][4 * u + 3])),
+                             f2_pack(k4.z, k4.w)),
+                        a2, a3);
+              s[c][4 * u] = __float_as_uint(a0);
+              s[c][4 * u + 1] = __float_as_uint(a1);
+              s[c][4 * u + 2] = __float_as_uint(a2);
+              s[c][4 * u + 3] = __float_as_uint(a3);
+            }
+        }
 
         const int kv0 = j * kBlockN;
         if (kv0 + kBlockN > N || (CAUSAL && kv0 + kBlockN - 1 > q_first)) {
@@ -491,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_use = fminf(m_use, m_new + 64.f / scale_log2);
           }
         }
-        const float neg_ms = -m_use * scale_log2;
-        const float alpha = ex2((m_norm - m_use) * scale_log2);
+        const float neg_ms = -m_use * c_row;
+        const float alpha = ex2((m_norm - m_use) * c_row);
         s_alpha[t * 128 + r] = alpha;
         mbar_arrive(&bar_alpha[t * 4 + (warp & 3)]);  // the correction warp rescales O_t meanwhile
         // Eight partial row sums held as four packed pairs: element e of the
@@ -501,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t sums2[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) sums2[u] = 0ull;
-        const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+        const uint64_t c2 = f2_pack(c_row, c_row);
         const uint64_t nm2 = f2_pack(neg_ms, neg_ms);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -600,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (qi < N) lse[(size_t)it.bh * N + qi] = m_norm * scale + logf(l_run);
+      if (qi < N) lse[(size_t)it.bh * N + qi] = m_norm * (I8 ? scale * sq : scale) + logf(l_run);
     }
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
   }
@@ -613,13 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool STABLE>
+template <int D, bool CAUSAL, bool STABLE, bool I8 = false>
 cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, const CUtensorMap& mo, void* o, float* lse,
-                            float beta,
-                            cudaStream_t stream) {
+                            float beta, cudaStream_t stream, const float* qs = nullptr,
+                            const float* ks = nullptr) {
   using C = FwdCfg<D>;
-  auto kernel = fwd_bf16_kernel<D, CAUSAL, STABLE>;
+  auto kernel = fwd_bf16_kernel<D, CAUSAL, STABLE, I8>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -632,7 +665,8 @@ cudaError_t launch_fwd_impl(const Problem& p, const CUtensorMap& mq, const CUten
   const int grid = sms > 0 ? std::min(total, sms) : total;
   const float scale_log2 = p.scale * 1.4426950408889634f;
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mo,
-                    static_cast<uint16_t*>(o), lse, BH, p.N, num_qt, p.scale, scale_log2, beta);
+                    static_cast<uint16_t*>(o), lse, BH, p.N, num_qt, p.scale, scale_log2, beta, qs,
+                    ks, n_pad(p.N));
 }
 
 }  // namespace
@@ -658,6 +692,21 @@ cudaError_t launch_fwd_bf16(const Problem& p, const void* q, const void* k, cons
   ATTN_FWD_CASE(64, false, true)
 #undef ATTN_FWD_CASE
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_int8_as_bf16(const Problem& p, const void* qc, const float* qs,
+                                    const void* kc, const float* ks, const void* v, void* o,
+                                    float* lse, cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_tmap_bhnd(&mq, qc, BH, p.N, p.d) || !make_tmap_bhnd(&mk, kc, BH, p.N, p.d) ||
+      !make_tmap_bhnd(&mv, v, BH, p.N, p.d) || !make_tmap_bhnd(&mo, o, BH, p.N, p.d))
+    return cudaErrorInvalidValue;
+  if (p.d == 128)
+    return p.causal ? launch_fwd_impl<128, true, false, true>(p, mq, mk, mv, mo, o, lse, 0.f, stream, qs, ks)
+                    : launch_fwd_impl<128, false, false, true>(p, mq, mk, mv, mo, o, lse, 0.f, stream, qs, ks);
+  return p.causal ? launch_fwd_impl<64, true, false, true>(p, mq, mk, mv, mo, o, lse, 0.f, stream, qs, ks)
+                  : launch_fwd_impl<64, false, false, true>(p, mq, mk, mv, mo, o, lse, 0.f, stream, qs, ks);
 }
 
 cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream) {

@@ -91,11 +91,15 @@ __device__ __forceinline__ void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, ui
 // codes rint(x / s) clamped to +-127 (rint: half to even), zero row -> 0.
 constexpr int kQuantRowsPerWarp = 4;  // rows loaded up front per warp (memory-level parallelism)
 
-template <int D>
+// BF16_CODES: codes written as BF16 values (exact integers) and scales in the
+// padded per-head layout [B*H][n_pad] (n_pad = N rounded up to 128), whose
+// padding the warp of each head's last row zeroes; otherwise int8 codes and
+// scales [B*H*N].
+template <int D, bool BF16_CODES>
 __global__ void __launch_bounds__(256) quantize_int8_kernel(const uint16_t* __restrict__ x,
-                                                            int8_t* __restrict__ codes,
+                                                            void* __restrict__ codes_out,
                                                             float* __restrict__ scales,
-                                                            long long rows) {
+                                                            long long rows, int N, int n_pad) {
   constexpr int kPer = D / 32;  // values per lane: 4 (one 8-byte load) or 2 (one 4-byte load)
   constexpr int R = kQuantRowsPerWarp;
   const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * R;
@@ -129,17 +133,34 @@ __global__ void __launch_bounds__(256) quantize_int8_kernel(const uint16_t* __re
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const float s = amax / 127.f;
     uint32_t packed = 0;
+    uint32_t bf[kPer / 2];  // codes as BF16 pairs (an integer |c| <= 127 is exact in BF16)
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
       const float r = s > 0.f ? rintf(v[e] / s) : 0.f;
-      const int c = static_cast<int>(fminf(fmaxf(r, -127.f), 127.f));
+      const float cf = fminf(fmaxf(r, -127.f), 127.f);
+      const int c = static_cast<int>(cf);
       packed |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+      if (e & 1) bf[e >> 1] = pack_bf16x2(__uint_as_float(bf[e >> 1]), cf);
+      else bf[e >> 1] = __float_as_uint(cf);
     }
-    if constexpr (kPer == 4)
-      *reinterpret_cast<uint32_t*>(codes + row * D + lane * kPer) = packed;
-    else
-      *reinterpret_cast<uint16_t*>(codes + row * D + lane * kPer) = static_cast<uint16_t>(packed);
-    if (lane == 0) scales[row] = s;
+    if constexpr (BF16_CODES) {
+      uint16_t* codes = static_cast<uint16_t*>(codes_out);
+      if constexpr (kPer == 4)
+        *reinterpret_cast<uint2*>(codes + row * D + lane * kPer) = make_uint2(bf[0], bf[1]);
+      else
+        *reinterpret_cast<uint32_t*>(codes + row * D + lane * kPer) = bf[0];
+      const long long bh = row / N, n = row - bh * N;
+      if (lane == 0) scales[bh * n_pad + n] = s;
+      if (n == N - 1)  // this head's padded scale entries
+        for (int z = N + lane; z < n_pad; z += 32) scales[bh * n_pad + z] = 0.f;
+    } else {
+      int8_t* codes = static_cast<int8_t*>(codes_out);
+      if constexpr (kPer == 4)
+        *reinterpret_cast<uint32_t*>(codes + row * D + lane * kPer) = packed;
+      else
+        *reinterpret_cast<uint16_t*>(codes + row * D + lane * kPer) = static_cast<uint16_t>(packed);
+      if (lane == 0) scales[row] = s;
+    }
   }
 }
 
@@ -360,12 +381,25 @@ cudaError_t launch_quantize_int8(const Problem& p, const void* x, void* codes, f
   const long long rows = (long long)p.B * p.H * p.N;
   const long long per_block = 8LL * kQuantRowsPerWarp;
   const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
+  const auto* xx = static_cast<const uint16_t*>(x);
   if (p.d == 128)
-    quantize_int8_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x),
-                                                          static_cast<int8_t*>(codes), scales, rows);
+    quantize_int8_kernel<128, false><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, p.N);
   else
-    quantize_int8_kernel<64><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x),
-                                                         static_cast<int8_t*>(codes), scales, rows);
+    quantize_int8_kernel<64, false><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, p.N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_int8_as_bf16(const Problem& p, const void* x, void* codes,
+                                         float* scales, cudaStream_t stream) {
+  const long long rows = (long long)p.B * p.H * p.N;
+  const long long per_block = 8LL * kQuantRowsPerWarp;
+  const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
+  const auto* xx = static_cast<const uint16_t*>(x);
+  const int np = n_pad(p.N);
+  if (p.d == 128)
+    quantize_int8_kernel<128, true><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, np);
+  else
+    quantize_int8_kernel<64, true><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, np);
   return cudaGetLastError();
 }
 

@@ -95,3 +95,72 @@ def test_int8_inputs_reject_wrong_dtype(A):
     s = torch.zeros(1, 1, 64, dtype=torch.float32, device="cuda")
     with pytest.raises(ValueError):
         A.attn_fwd_int8(v, s, v, s, v)  # BF16 where INT8 codes are expected
+
+
+# ---------------------------------------------------------------------------
+# INT8 codes held in BF16: attn_quantize_int8_as_bf16 / attn_fwd_int8_as_bf16
+# (the tcgen05 path).  The codes are the same integers, so they must equal the
+# int8 codes exactly; the forward meets the same tolerances against the same
+# INT8 oracle.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(1, 1, 5, 64), (2, 3, 129, 128), (1, 2, 1000, 64)])
+def test_quantize_as_bf16_equals_int8_codes(A, shape):
+    B, H, N, d = shape
+    x = inputs.random_qkv(23, *shape)["q"]
+    x.reshape(-1, d)[2] = 0  # a zero row
+    xd = _bf16_dev(x)
+    c8, s8 = A.attn_quantize_int8(xd)
+    cb, sb = A.attn_quantize_int8_as_bf16(xd)
+    assert torch.equal(cb.float(), c8.float())
+    n_pad = A.int8_scale_rows(N)
+    assert sb.shape == (B, H, n_pad)
+    assert torch.equal(sb[:, :, :N], s8)
+    assert bool((sb[:, :, N:] == 0).all())
+
+
+def _check_int8_as_bf16_forward(A, x, B, H, N, d, scale, causal, heads=None):
+    t = {k: _bf16_dev(v) for k, v in x.items()}
+    qc, qs = A.attn_quantize_int8_as_bf16(t["q"])
+    kc, ks = A.attn_quantize_int8_as_bf16(t["k"])
+    o, lse = A.attn_fwd_int8_as_bf16(qc, qs, kc, ks, t["v"], scale=scale, causal=causal)
+    A.attn_check_status()
+    assert bool(torch.isfinite(o.float()).all())
+    f = {k: inputs.bf16_bits_to_f32(v).reshape(B * H, N, d) for k, v in x.items()}
+    o = o.float().cpu().numpy().reshape(B * H, N, d)
+    lse = lse.cpu().numpy().reshape(B * H, N)
+    for h in (range(B * H) if heads is None else heads):
+        o_ref, lse_ref = oi.int8_forward(f["q"][h], f["k"][h], f["v"][h], scale, causal)
+        e = deviation(o[h], o_ref)
+        assert e["max_abs"] <= 2e-2 and e["mean_abs"] <= 2e-3, (h, e)
+        assert deviation(lse[h], lse_ref)["max_abs"] <= 1e-3, h
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 1, 1, 64), (1, 2, 64, 128), (2, 1, 129, 64),
+                                   (1, 2, 333, 128), (1, 1, 1024, 64), (1, 1, 700, 128)])
+def test_int8_as_bf16_forward_matches_oracle(A, shape, causal):
+    B, H, N, d = shape
+    x = inputs.random_qkv(31, B, H, N, d)
+    _check_int8_as_bf16_forward(A, x, B, H, N, d, d ** -0.5, causal)
+
+
+def test_int8_as_bf16_forward_zero_query_row(A):
+    """A row of zero codes scores 0 against every key: uniform weights over the visible keys."""
+    B, H, N, d = 1, 1, 200, 64
+    x = inputs.random_qkv(33, B, H, N, d)
+    x["q"][0, 0, 150] = 0
+    _check_int8_as_bf16_forward(A, x, B, H, N, d, d ** -0.5, True)
+
+
+def test_int8_as_bf16_forward_llama7b_shape(A):
+    w = inputs.WORKLOADS["llama7b"]
+    x = inputs.make_inputs(w, seed=0)
+    _check_int8_as_bf16_forward(A, x, w.B, w.H, w.N, w.d, w.scale, w.causal,
+                                heads=[0, w.B * w.H - 1])
+
+
+def test_int8_as_bf16_rejects_unpadded_scales(A):
+    c = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16, device="cuda")
+    s = torch.zeros(1, 1, 64, dtype=torch.float32, device="cuda")  # [B, H, N], not [B, H, N_pad]
+    with pytest.raises(ValueError):
+        A.attn_fwd_int8_as_bf16(c, s, c, s, c)
