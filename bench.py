@@ -490,10 +490,12 @@ def run_deviation(args):
 # ---------------------------------------------------------------------------
 def run_int8_forward(args, w):
     """One JSON line for the INT8-input forward: a step quantizes Q and K
-    (attn_quantize_int8) and runs attn_fwd_int8; value = forward FLOP count
-    (4*B*H*N^2*d, halved when causal) per second.  Next to it: the BF16
-    forward's time, and both forwards' deviation from the FP64 definition on
-    head (0,0) (the INT8 one also against the INT8 oracle)."""
+    (attn_quantize_int8_as_bf16) and runs attn_fwd_int8_as_bf16, the tcgen05
+    path; value = forward FLOP count (4*B*H*N^2*d, halved when causal) per
+    second.  Next to it: the same step on int8 codes (attn_quantize_int8 +
+    attn_fwd_int8, the mma.sync path), the BF16 forward's time, and the
+    forwards' deviation from the FP64 definition on head (0,0) (the INT8 ones
+    also against the INT8 oracle)."""
     import torch
 
     import oracle
@@ -504,6 +506,9 @@ def run_int8_forward(args, w):
     build.build()
     x = inputs.make_inputs(w, seed=0)
     t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in x.items()}
+    qc, qcs = attn.attn_quantize_int8_as_bf16(t["q"])
+    kc, kcs = attn.attn_quantize_int8_as_bf16(t["k"])
+    oc, lc = attn.attn_fwd_int8_as_bf16(qc, qcs, kc, kcs, t["v"], scale=w.scale, causal=w.causal)
     q8, qs = attn.attn_quantize_int8(t["q"])
     k8, ks = attn.attn_quantize_int8(t["k"])
     o8, l8 = attn.attn_fwd_int8(q8, qs, k8, ks, t["v"], scale=w.scale, causal=w.causal)
@@ -511,6 +516,12 @@ def run_int8_forward(args, w):
     stream = torch.cuda.current_stream()
 
     def step():
+        attn.attn_quantize_int8_as_bf16(t["q"], qc, qcs)
+        attn.attn_quantize_int8_as_bf16(t["k"], kc, kcs)
+        attn.attn_fwd_int8_as_bf16(qc, qcs, kc, kcs, t["v"], scale=w.scale, causal=w.causal, o=oc,
+                                   lse=lc)
+
+    def step_s8():
         attn.attn_quantize_int8(t["q"], q8, qs)
         attn.attn_quantize_int8(t["k"], k8, ks)
         attn.attn_fwd_int8(q8, qs, k8, ks, t["v"], scale=w.scale, causal=w.causal, o=o8, lse=l8)
@@ -529,22 +540,29 @@ def run_int8_forward(args, w):
 
     steps = max(1, min(args.steps, 200))
     ms = timed(step, steps)
+    ms_s8 = timed(step_s8, steps)
     ms_bf16 = timed(lambda: attn.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal,
                                           o=ob, lse=lb), steps)
     attn.attn_check_status()
     f = {k: inputs.bf16_bits_to_f32(v.reshape(w.B * w.H, w.N, w.d)[0]) for k, v in x.items()}
     o_ref, _ = oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
     o_i8ref, _ = oi.int8_forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+    och = oc.reshape(w.B * w.H, w.N, w.d)[0].float().cpu().numpy()
     o8h = o8.reshape(w.B * w.H, w.N, w.d)[0].float().cpu().numpy()
     obh = ob.reshape(w.B * w.H, w.N, w.d)[0].float().cpu().numpy()
     line = {"metric": "INT8-input attention forward TFLOP/s-equivalent on 1 GB300",
             "value": w.fwd_flops() / ms / 1e9, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "dtype": "s8 (Q K^T), bf16 (P V)", "data": "synthetic", "config": _config(w),
-            "step": "attn_quantize_int8 on Q and K + attn_fwd_int8",
+            "dtype": "int8 codes held in bf16 (exact integer Q K^T), bf16 (P V)",
+            "data": "synthetic", "config": _config(w),
+            "step": "attn_quantize_int8_as_bf16 on Q and K + attn_fwd_int8_as_bf16",
+            "int8_codes_mma_sync": {"ms": ms_s8, "tflops": w.fwd_flops() / ms_s8 / 1e9,
+                                    "step": "attn_quantize_int8 on Q and K + attn_fwd_int8"},
             "bf16_forward": {"ms": ms_bf16, "tflops": w.fwd_flops() / ms_bf16 / 1e9},
-            "o_vs_fp64": {"int8": deviation(o8h, o_ref), "bf16": deviation(obh, o_ref)},
-            "o_int8_vs_int8_oracle": deviation(o8h, o_i8ref)}
+            "o_vs_fp64": {"int8_as_bf16": deviation(och, o_ref), "int8": deviation(o8h, o_ref),
+                          "bf16": deviation(obh, o_ref)},
+            "o_int8_vs_int8_oracle": {"int8_as_bf16": deviation(och, o_i8ref),
+                                      "int8": deviation(o8h, o_i8ref)}}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -87,79 +87,78 @@ __device__ __forceinline__ void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, ui
 }
 
 // ----------------------------------------------------------------- quantize
-// One warp per row of d values: FP32 max|x| by shuffles, s = max / 127,
-// codes rint(x / s) clamped to +-127 (rint: half to even), zero row -> 0.
-constexpr int kQuantRowsPerWarp = 4;  // rows loaded up front per warp (memory-level parallelism)
-
+// Each lane handles 16-byte units (8 values): a row of d values is D/8 lanes
+// (16 at d = 128, 8 at d = 64), so one warp load covers 32 / (D/8) rows, and
+// a warp keeps kQuantGroups such row groups in flight.  FP32 max|x| by
+// shuffles inside the row's lane group, s = max / 127, codes rint(x / s)
+// clamped to +-127 (rint: half to even), zero row -> 0.
+//
 // BF16_CODES: codes written as BF16 values (exact integers) and scales in the
 // padded per-head layout [B*H][n_pad] (n_pad = N rounded up to 128), whose
-// padding the warp of each head's last row zeroes; otherwise int8 codes and
+// padding the lanes of each head's last row zero; otherwise int8 codes and
 // scales [B*H*N].
+constexpr int kQuantGroups = 4;
+template <int D>
+constexpr long long quant_rows_per_block() {
+  return 8LL * kQuantGroups * (32 / (D / 8));
+}
 template <int D, bool BF16_CODES>
 __global__ void __launch_bounds__(256) quantize_int8_kernel(const uint16_t* __restrict__ x,
                                                             void* __restrict__ codes_out,
                                                             float* __restrict__ scales,
                                                             long long rows, int N, int n_pad) {
-  constexpr int kPer = D / 32;  // values per lane: 4 (one 8-byte load) or 2 (one 4-byte load)
-  constexpr int R = kQuantRowsPerWarp;
-  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * R;
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerLoad = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
-  uint32_t w[R][kPer / 2];  // BF16 pairs of R rows
+  const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
+  const long long warp_global = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long row_base = warp_global * (kQuantGroups * kRowsPerLoad);
+  uint4 w[kQuantGroups];
 #pragma unroll
-  for (int q = 0; q < R; ++q) {
-    const long long row = row0 + q;
-    if (row >= rows) break;
-    if constexpr (kPer == 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(x + row * D + lane * kPer);
-      w[q][0] = u.x;
-      w[q][1] = u.y;
-    } else {
-      w[q][0] = *reinterpret_cast<const uint32_t*>(x + row * D + lane * kPer);
-    }
+  for (int q = 0; q < kQuantGroups; ++q) {
+    const long long row = row_base + q * kRowsPerLoad + sub;
+    w[q] = row < rows ? *reinterpret_cast<const uint4*>(x + row * D + part * 8)
+                      : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
-  for (int q = 0; q < R; ++q) {
-    const long long row = row0 + q;
-    if (row >= rows) break;  // uniform across the warp
-    float v[kPer];
+  for (int q = 0; q < kQuantGroups; ++q) {
+    const long long row = row_base + q * kRowsPerLoad + sub;
+    const uint32_t u[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+    float v[8];
     float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      v[e] = __uint_as_float(e & 1 ? (w[q][e >> 1] & 0xFFFF0000u) : (w[q][e >> 1] << 16));
+    for (int e = 0; e < 8; ++e) {
+      v[e] = __uint_as_float(e & 1 ? (u[e >> 1] & 0xFFFF0000u) : (u[e >> 1] << 16));
       amax = fmaxf(amax, fabsf(v[e]));
     }
+    // All lanes take part (rows past the end hold zeros); the xor offsets stay
+    // inside the row's aligned group of kLanesPerRow lanes.
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (row >= rows) continue;
     const float s = amax / 127.f;
-    uint32_t packed = 0;
-    uint32_t bf[kPer / 2];  // codes as BF16 pairs (an integer |c| <= 127 is exact in BF16)
+    uint32_t packed[2] = {0u, 0u};
+    uint32_t bf[4];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
+    for (int e = 0; e < 8; ++e) {
       const float r = s > 0.f ? rintf(v[e] / s) : 0.f;
       const float cf = fminf(fmaxf(r, -127.f), 127.f);
-      const int c = static_cast<int>(cf);
-      packed |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+      packed[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(cf)) & 0xFFu) << (8 * (e & 3));
       if (e & 1) bf[e >> 1] = pack_bf16x2(__uint_as_float(bf[e >> 1]), cf);
       else bf[e >> 1] = __float_as_uint(cf);
     }
     if constexpr (BF16_CODES) {
       uint16_t* codes = static_cast<uint16_t*>(codes_out);
-      if constexpr (kPer == 4)
-        *reinterpret_cast<uint2*>(codes + row * D + lane * kPer) = make_uint2(bf[0], bf[1]);
-      else
-        *reinterpret_cast<uint32_t*>(codes + row * D + lane * kPer) = bf[0];
+      *reinterpret_cast<uint4*>(codes + row * D + part * 8) = make_uint4(bf[0], bf[1], bf[2], bf[3]);
       const long long bh = row / N, n = row - bh * N;
-      if (lane == 0) scales[bh * n_pad + n] = s;
+      if (part == 0) scales[bh * n_pad + n] = s;
       if (n == N - 1)  // this head's padded scale entries
-        for (int z = N + lane; z < n_pad; z += 32) scales[bh * n_pad + z] = 0.f;
+        for (int z = N + part; z < n_pad; z += kLanesPerRow) scales[bh * n_pad + z] = 0.f;
     } else {
       int8_t* codes = static_cast<int8_t*>(codes_out);
-      if constexpr (kPer == 4)
-        *reinterpret_cast<uint32_t*>(codes + row * D + lane * kPer) = packed;
-      else
-        *reinterpret_cast<uint16_t*>(codes + row * D + lane * kPer) = static_cast<uint16_t>(packed);
-      if (lane == 0) scales[row] = s;
+      *reinterpret_cast<uint2*>(codes + row * D + part * 8) = make_uint2(packed[0], packed[1]);
+      if (part == 0) scales[row] = s;
     }
   }
 }
@@ -379,27 +378,33 @@ cudaError_t launch_int8_impl(const Problem& p, const int8_t* q8, const float* qs
 cudaError_t launch_quantize_int8(const Problem& p, const void* x, void* codes, float* scales,
                                  cudaStream_t stream) {
   const long long rows = (long long)p.B * p.H * p.N;
-  const long long per_block = 8LL * kQuantRowsPerWarp;
-  const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
   const auto* xx = static_cast<const uint16_t*>(x);
-  if (p.d == 128)
-    quantize_int8_kernel<128, false><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, p.N);
-  else
-    quantize_int8_kernel<64, false><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, p.N);
+  if (p.d == 128) {
+    constexpr long long per = quant_rows_per_block<128>();
+    quantize_int8_kernel<128, false><<<(unsigned)((rows + per - 1) / per), 256, 0, stream>>>(
+        xx, codes, scales, rows, p.N, p.N);
+  } else {
+    constexpr long long per = quant_rows_per_block<64>();
+    quantize_int8_kernel<64, false><<<(unsigned)((rows + per - 1) / per), 256, 0, stream>>>(
+        xx, codes, scales, rows, p.N, p.N);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_int8_as_bf16(const Problem& p, const void* x, void* codes,
                                          float* scales, cudaStream_t stream) {
   const long long rows = (long long)p.B * p.H * p.N;
-  const long long per_block = 8LL * kQuantRowsPerWarp;
-  const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
   const auto* xx = static_cast<const uint16_t*>(x);
   const int np = n_pad(p.N);
-  if (p.d == 128)
-    quantize_int8_kernel<128, true><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, np);
-  else
-    quantize_int8_kernel<64, true><<<blocks, 256, 0, stream>>>(xx, codes, scales, rows, p.N, np);
+  if (p.d == 128) {
+    constexpr long long per = quant_rows_per_block<128>();
+    quantize_int8_kernel<128, true><<<(unsigned)((rows + per - 1) / per), 256, 0, stream>>>(
+        xx, codes, scales, rows, p.N, np);
+  } else {
+    constexpr long long per = quant_rows_per_block<64>();
+    quantize_int8_kernel<64, true><<<(unsigned)((rows + per - 1) / per), 256, 0, stream>>>(
+        xx, codes, scales, rows, p.N, np);
+  }
   return cudaGetLastError();
 }
 
