@@ -126,8 +126,9 @@ ATTN_API attn_status attn_quantize_int8(const void* x, void* codes, float* scale
  * integer dot product exact, then the FP32 online softmax and P V (P rounded
  * to BF16), O = softmax(S [+mask]) V and LSE = ln sum_j exp(S_ij) as in
  * attn_fwd.  sm_103a has no INT8 tcgen05 MMA, so this path runs on the
- * warp-level mma.sync tensor-core instructions and is slower than attn_fwd;
- * it exists for the numerics of INT8 inputs.
+ * warp-level mma.sync tensor-core instructions and is several times slower
+ * than attn_fwd; attn_fwd_int8_as_bf16 computes the same scores on the
+ * tcgen05 path from codes held in BF16.
  *   q8, k8  : [B,H,N,d] int8, device.   q_scale, k_scale : [B,H,N] FP32.
  *   v       : [B,H,N,d] BF16.           o : [B,H,N,d] BF16.   lse : [B,H,N] FP32.
  * d in {64, 128}; all pointers 16-byte aligned, device memory.

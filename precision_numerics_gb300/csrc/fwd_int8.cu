@@ -11,7 +11,10 @@
 //   as in the BF16 forward, O = P V / l and LSE = m + ln l.
 //
 // sm_103a has no INT8 form of tcgen05.mma (ptxas rejects kind::i8 for this
-// target), so the contractions use the warp-level tensor-core path:
+// target).  The fast path is attn_fwd_int8_as_bf16: the same codes held in
+// BF16 run through the tcgen05 forward of fwd_bf16.cu, where every product
+// and partial sum of the integer dot product is exact in FP32.  For int8
+// codes, this file's kernel uses the warp-level tensor-core path:
 // mma.sync m16n8k32 s8 for Q K^T and m16n8k16 bf16 for P V.  CTA = 64 query
 // rows of one (b, h), 4 warps x 16 rows; key tiles of 64 rows stream through
 // a two-stage cp.async ring.  Each thread holds rows g and g+8 of its warp's
