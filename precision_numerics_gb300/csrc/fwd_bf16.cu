@@ -74,11 +74,19 @@ struct FwdCfg {
   // d = 128 the direct stores were ~1.5% slower).
   static constexpr bool kStagedOut = (D == 128);
   static constexpr int kOffStage = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffStage + (kStagedOut ? 2 * kChunkBytes : 0);
+  // INT8 variant: the key scales of each K tile (128 FP32) in a ring of their
+  // own, with a full barrier per slot.  Slot g % kKsSlots is refilled for key
+  // tile g + kKsSlots when K of that tile loads, which waits until the S
+  // products of tile g + 1 have completed; those were issued only once both
+  // softmax warpgroups had finished tile g.  So the slot's previous scales
+  // have been read, and no softmax warp falls two phases behind its barrier.
+  static constexpr int kKsSlots = kStages + 1;
+  static constexpr int kOffKs = kOffStage + (kStagedOut ? 2 * kChunkBytes : 0);
+  static constexpr int kOffBar = kOffKs + kKsSlots * 128 * 4;
   // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
   // p_full[2], o_done[2], mma_final, alpha[2][4] (one per tile and softmax
-  // warp), epi_full[2], epi_free[2]
-  static constexpr int kNumBars = 2 + 4 * kStages + 19;
+  // warp), epi_full[2], epi_free[2], ks_full[kKsSlots]
+  static constexpr int kNumBars = 2 + 4 * kStages + 19 + kKsSlots;
   static constexpr int kOffAlpha = kOffBar + kNumBars * 8 + 16;  // FP32 [2][128]
   static constexpr int kSmemBytes = kOffAlpha + 2 * 128 * 4;
   static constexpr uint32_t kTmemCols = 512;
@@ -156,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_alpha = bar_final + 1;
   uint64_t* bar_epifull = bar_alpha + 8;  // a staged O chunk is complete
   uint64_t* bar_epifree = bar_epifull + 2;  // its TMA store has read the staging slot
+  uint64_t* bar_ksfull = bar_epifree + 2;  // INT8: a key-scale slot has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   float* s_alpha = reinterpret_cast<float*>(smem + C::kOffAlpha);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -180,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_epifull[t], 128);
       mbar_init(&bar_epifree[t], 1);
     }
+    for (int k = 0; k < C::kKsSlots; ++k) mbar_init(&bar_ksfull[k], 1);
     mbar_init(bar_final, 1);
     fence_mbar_init();
   }
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       bool ok = true;
-      int g = 0, items = 0, issued_k = 0, issued_v = 0;
+      int g = 0, items = 0, issued_k = 0, issued_v = 0, issued_ks = 0;
       for (int r = 0; ok; ++r) {
         const int L = item_of(r, total);
         if (L < 0) break;
@@ -232,6 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(sK + st * C::kTileBytes + c * C::kChunkBytes, &tmK, &bar_kfull[st], c * 64,
                         j * kBlockN, it.bh);
+          if constexpr (I8) {
+            uint64_t* kb = &bar_ksfull[g % C::kKsSlots];
+            mbar_arrive_expect_tx(kb, 128 * 4);
+            bulk_load(smem + C::kOffKs + (g % C::kKsSlots) * 128 * 4,
+                      ks + (size_t)it.bh * Npad + j * kBlockN, 128 * 4, kb);
+            issued_ks = g + 1;
+          }
           issued_k = g + 1;
           if (use > 0 && !mbar_wait(&bar_vempty[st], (use - 1) & 1)) { ok = false; break; }
           mbar_arrive_expect_tx(&bar_vfull[st], C::kTileBytes);
@@ -248,6 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bar_kfull[x % C::kStages], (x / C::kStages) & 1);
       for (int x = max(0, issued_v - C::kStages); x < issued_v; ++x)
         mbar_wait(&bar_vfull[x % C::kStages], (x / C::kStages) & 1);
+      for (int x = max(0, issued_ks - C::kKsSlots); x < issued_ks; ++x)
+        mbar_wait(&bar_ksfull[x % C::kKsSlots], (x / C::kKsSlots) & 1);
     } else if (warp == 1 && !abort_all) {
       // ------------------------------------------------------------ MMA issuer
       // The whole warp runs this role with warp-uniform operands; elect.sync
@@ -433,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = !abort_all;
     int sc = 0;  // S_t tiles consumed so far (s_full phases)
     int oc = 0;  // items whose O_t was completed so far (o_done phases)
+    int gbase = 0;  // K/V ring position of the item's first key tile
     int es = 0;  // O chunks stored so far (epi_full / epi_free phases)
     for (int rr = 0; ok; ++rr) {
       const int L = item_of(rr, total);
@@ -461,14 +481,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence(s[c]);
         if constexpr (I8) {
-          // S_ij * ks_j: the key scales of this tile (128 FP32, 16-byte aligned in
-          // the padded layout; the entries past N belong to masked keys).
-          const float4* kr = reinterpret_cast<const float4*>(ks + (size_t)it.bh * Npad + j * kBlockN);
+          // S_ij * ks_j: the key scales of this tile from the scale ring (entries
+          // past N belong to masked keys).
+          const int gk = gbase + j;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bar_ksfull[gk % C::kKsSlots], (gk / C::kKsSlots) & 1));
+          if (!ok) break;
+          const float4* kr =
+              reinterpret_cast<const float4*>(smem + C::kOffKs + (gk % C::kKsSlots) * 128 * 4);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const float4 k4 = __ldg(kr + c * 8 + u);
+              const float4 k4 = kr[c * 8 + u];
               float a0, a1, a2, a3;
               f2_unpack(mul2(f2_pack(__uint_as_float(s[c][4 * u]), __uint_as_float(s[c][4 * u + 1])),
                              f2_pack(k4.x, k4.y)),
@@ -565,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_norm = m_use;
       }
       sc += n;
+      gbase += it.nmax;
       if (!ok || n == 0) continue;
       // ------------------------------------------------------------ epilogue
       // O = O_acc / l, rounded to BF16, staged one 64-column chunk at a time in
