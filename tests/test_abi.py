@@ -110,3 +110,29 @@ def test_stable_forward_argument_checks(lib):
     assert call(1.0) == attn.ATTN_ERR_INVALID_ARG
     assert call(float("inf")) == attn.ATTN_ERR_INVALID_ARG
     assert call(2.0, dt=1) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_int8_entry_points_check_arguments_before_any_launch(lib):
+    """Shape, scale and pointer errors of the four INT8 entry points come back synchronously."""
+    f = ctypes.c_float
+    for name in ("attn_quantize_int8", "attn_quantize_int8_as_bf16"):
+        fn = getattr(lib, name)
+        assert fn(16, 16, 16, 1, 1, 128, 96, None) == attn.ATTN_ERR_UNSUPPORTED  # d
+        assert fn(16, 16, 16, 1, 1, 0, 64, None) == attn.ATTN_ERR_INVALID_ARG  # N
+        assert fn(None, 16, 16, 1, 1, 128, 64, None) == attn.ATTN_ERR_INVALID_ARG  # null x
+        assert "NULL" in lib.attn_last_error().decode()
+        assert fn(16, 16, 16 * 7 + 4, 1, 1, 128, 64, None) == attn.ATTN_ERR_INVALID_ARG  # misaligned
+    for name in ("attn_fwd_int8", "attn_fwd_int8_as_bf16"):
+        fn = getattr(lib, name)
+
+        def call(*, q=16, ks=16, d=64, scale=0.125):
+            return fn(q, 16, 16, ks, 16, 16, 16, 1, 1, 128, d, f(scale), 1, None)
+        assert call(d=96) == attn.ATTN_ERR_UNSUPPORTED
+        assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+        assert call(scale=0.0) == attn.ATTN_ERR_INVALID_ARG
+        assert call(q=None) == attn.ATTN_ERR_INVALID_ARG
+        assert call(ks=16 * 5 + 8) == attn.ATTN_ERR_INVALID_ARG  # misaligned k scales
+
+
+def test_int8_padded_scale_rows():
+    assert [attn.int8_scale_rows(n) for n in (1, 127, 128, 129, 4096)] == [128, 128, 128, 256, 4096]
