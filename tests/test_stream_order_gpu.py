@@ -52,7 +52,7 @@ def _chain(A, t, rounds, sync, causal, scale):
         out.append({k: v.clone() for k, v in (("o1", o1), ("o2", o2), ("lse2", lse2),
                                                ("dq", dq), ("dk", dk), ("dv", dv),
                                                ("o3", o3), ("lse3", lse3))})
-        q = o3  # the next round starts from this round's last output
+        q = o3  # the next link of the chain starts from this link's last output
     torch.cuda.synchronize()
     A.attn_check_status()
     return out
