@@ -38,7 +38,9 @@ key/value permutation, causal prefixes), library routines (SciPy
 log-sum-exp and softmax, PyTorch FP64 scaled-dot-product attention with
 autograd), central finite differences of L = sum(dO o O), and a
 pure-Python brute force on tiny inputs.  The naive BF16 comparator's
-rounding is pinned against PyTorch's BF16 conversion.
+rounding is pinned against PyTorch's BF16 conversion, and where it rounds
+against an eager framework's BF16 graph: PyTorch CPU ops on BF16 tensors and
+their autograd backward give the same BF16 values (at least 99% bit for bit).
 """
 from __future__ import annotations
 

@@ -280,6 +280,85 @@ def test_naive_bf16_within_bf16_error_of_exact(causal):
         assert np.linalg.norm(y - x) / np.linalg.norm(x) < 0.03
 
 
+def _eager_bf16_autograd(q, k, v, do, scale, causal):
+    """The same attention run by an eager framework: PyTorch on the CPU on
+    BF16 tensors (each op returns a BF16 tensor), differentiated by autograd."""
+    torch = pytest.importorskip("torch")
+
+    def leaf(x):
+        return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).requires_grad_(True)
+
+    qt, kt, vt = leaf(q), leaf(k), leaf(v)
+    s = (qt @ kt.T) * scale
+    if causal:
+        hidden = torch.ones(s.shape, dtype=torch.bool).triu(1)
+        s = s.masked_fill(hidden, float("-inf"))
+    o = torch.softmax(s, -1) @ vt
+    o.backward(torch.from_numpy(np.asarray(do, np.float32)).to(torch.bfloat16))
+    return tuple(x.detach().float().numpy() for x in (o, qt.grad, kt.grad, vt.grad))
+
+
+def _naive_forward_p_unrounded(q, k, v, scale, causal):
+    """A plausible slip: probabilities kept in FP32 (no BF16 tensor between
+    the softmax and P V)."""
+    q, k, v = (np.asarray(x, np.float32) for x in (q, k, v))
+    s = oracle.round_bf16(oracle.round_bf16(q @ k.T) * np.float32(scale))
+    if causal:
+        s = np.where(np.triu(np.ones(s.shape, bool), 1), np.float32(-np.inf), s)
+    e = np.exp(s - s.max(axis=1, keepdims=True), dtype=np.float32)
+    return oracle.round_bf16((e / e.sum(axis=1, keepdims=True, dtype=np.float32)) @ v)
+
+
+def _naive_backward_scale_folded(q, k, v, do, scale, causal):
+    """A plausible slip: the softmax scale folded into dS before its BF16
+    rounding (one rounding where the eager graph has two)."""
+    q, k, v, do = (np.asarray(x, np.float32) for x in (q, k, v, do))
+    s = oracle.round_bf16(oracle.round_bf16(q @ k.T) * np.float32(scale))
+    if causal:
+        s = np.where(np.triu(np.ones(s.shape, bool), 1), np.float32(-np.inf), s)
+    e = np.exp(s - s.max(axis=1, keepdims=True), dtype=np.float32)
+    p = oracle.round_bf16(e / e.sum(axis=1, keepdims=True, dtype=np.float32))
+    dp = oracle.round_bf16(do @ v.T)
+    ds = oracle.round_bf16(np.float32(scale) * p *
+                           (dp - (dp * p).sum(axis=1, keepdims=True, dtype=np.float32)))
+    return oracle.round_bf16(ds @ k), oracle.round_bf16(ds.T @ q)
+
+
+# (n, d, causal): d = 32 and 128 give softmax scales 1/sqrt(d) that are not
+# powers of two, so every BF16 rounding of a scaled tensor is visible (with
+# d = 64 the scale 1/8 is exact and two roundings in a row equal one).
+EAGER_CASES = [(96, 32, True), (128, 128, False)]
+
+
+@pytest.mark.parametrize("n,d,causal", EAGER_CASES)
+def test_naive_bf16_rounding_matches_eager_bf16_autograd(n, d, causal):
+    """Pins where the naive comparator rounds: an eager framework's BF16
+    graph (PyTorch CPU ops and autograd) gives the same BF16 values.  Not
+    every element can agree bit for bit (the two sum in different orders and
+    use different exp routines, which can move a value across a BF16
+    rounding boundary), so the pin is that at least 99% do, against 36-62%
+    when one rounding is dropped or merged (see the planted slips below)."""
+    q, k, v, do = (oracle.round_bf16(_rand(700 + s, n, d).astype(np.float32)) for s in range(4))
+    scale = 1 / math.sqrt(d)
+    o, _ = oracle.naive_bf16_forward(q, k, v, scale, causal)
+    dq, dk, dv = oracle.naive_bf16_backward(q, k, v, do, scale, causal)
+    eo, edq, edk, edv = _eager_bf16_autograd(q, k, v, do, scale, causal)
+    for name, x, y in (("o", o, eo), ("dq", dq, edq), ("dk", dk, edk), ("dv", dv, edv)):
+        assert np.mean(x == y) >= 0.99, name
+        assert np.abs(x - y).max() <= 2 ** -6 * np.abs(y).max(), name
+
+
+@pytest.mark.parametrize("n,d,causal", EAGER_CASES)
+def test_eager_pin_catches_misplaced_roundings(n, d, causal):
+    q, k, v, do = (oracle.round_bf16(_rand(700 + s, n, d).astype(np.float32)) for s in range(4))
+    scale = 1 / math.sqrt(d)
+    eo, edq, edk, _ = _eager_bf16_autograd(q, k, v, do, scale, causal)
+    assert np.mean(_naive_forward_p_unrounded(q, k, v, scale, causal) == eo) < 0.9
+    dq_bad, dk_bad = _naive_backward_scale_folded(q, k, v, do, scale, causal)
+    assert np.mean(dq_bad == edq) < 0.9
+    assert np.mean(dk_bad == edk) < 0.9
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _forward_missing_max(q, k, v, scale, causal):
