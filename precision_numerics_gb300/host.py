@@ -2,9 +2,10 @@
 
 Every (b, h) head is independent, so the B*H heads are split into
 contiguous groups and, for each group, a pipeline runs over three kinds of
-stream: the host->device copy of Q, K, V, dO, then attn_fwd and attn_bwd on
-the device, then the device->host copy of O and LSE (as soon as the forward
-is done) and of dQ, dK, dV.  The copies of one group overlap the kernels of
+stream: the host->device copy of Q, K, V, dO, then attn_fwd (as soon as Q,
+K and V have landed) and attn_bwd (once dO has too) on the device, then the
+device->host copy of O and LSE (as soon as the forward is done) and of dQ,
+dK, dV.  The copies of one group overlap the kernels of
 its neighbours, and the two copy directions overlap each other.  By default
 the whole pipeline is captured once as a CUDA graph and replayed.  All
 arithmetic runs in the library's kernels; this module only schedules copies
@@ -120,18 +121,24 @@ class HostAttention:
             # This group's device buffers are free once the previous run copied them out.
             if after_previous and self._last_out[g] is not None:
                 s_in.wait_event(self._last_out[g])
+            # The forward needs Q, K, V only; dO is still on its way while it runs.
             with torch.cuda.stream(s_in):
-                for name, src in (("q", q), ("k", k), ("v", v), ("do", do)):
+                for name, src in (("q", q), ("k", k), ("v", v)):
                     t[name].copy_(self._heads(src, a, b), non_blocking=True)
+                ev_qkv = torch.cuda.Event()
+                ev_qkv.record(s_in)
+                t["do"].copy_(self._heads(do, a, b), non_blocking=True)
                 ev_in = torch.cuda.Event()
                 ev_in.record(s_in)
             s_cmp = self.s_cmp[g % len(self.s_cmp)]
-            s_cmp.wait_event(ev_in)
+            s_cmp.wait_event(ev_qkv)
             with torch.cuda.stream(s_cmp):
                 attn.attn_fwd(t["q"], t["k"], t["v"], scale=self.scale, causal=self.causal,
                               o=t["o"], lse=t["lse"], stream=s_cmp)
                 ev_fwd = torch.cuda.Event()
                 ev_fwd.record(s_cmp)
+            s_cmp.wait_event(ev_in)
+            with torch.cuda.stream(s_cmp):
                 attn.attn_bwd(t["q"], t["k"], t["v"], t["o"], t["lse"], t["do"], scale=self.scale,
                               causal=self.causal, dq=t["dq"], dk=t["dk"], dv=t["dv"],
                               workspace=t["ws"], stream=s_cmp)
