@@ -327,9 +327,11 @@ def run_ours(args, w):
     # End-to-end through the public API with pinned host buffers: the head
     # groups are pipelined (H2D copy, kernels, D2H copy on their own streams),
     # captured once as a CUDA graph and replayed every step.
-    from precision_numerics_gb300.host import HostAttention
+    from precision_numerics_gb300.host import HostAttention, ramped_group_sizes
+    groups = (None if args.e2e_even_groups
+              else ramped_group_sizes(B * H, args.e2e_chunks))
     pipe = HostAttention(B, H, N, d, scale=w.scale, causal=w.causal, chunks=args.e2e_chunks,
-                         device=dev)
+                         group_sizes=groups, device=dev)
     for _ in range(max(3, min(args.warmup, 5))):
         pipe.run(host["q"], host["k"], host["v"], host["do"])
     e2e_steps = max(1, min(args.steps, 20))
@@ -388,7 +390,8 @@ def run_ours(args, w):
                          "traffic": _traffic_per_launch(w.name),
                          "algorithmic": "2.5 * 4*B*H*N^2*d/2 FLOP per launch (5 matmuls)"},
             "e2e": {"value": _job_tflops(world, step_flops, 1, e2e_ms), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "head_groups": [b - a for a, b in pipe.groups]},
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": sampler.summary(),
         }
@@ -580,7 +583,10 @@ def main():
                     help="print the numeric-deviation report instead of the bench line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=4,
-                    help="head groups pipelined in the end-to-end (host buffer) measurement")
+                    help="head groups pipelined in the end-to-end (host buffer) measurement; "
+                         "by default shifted by half a group (half-size first and last groups)")
+    ap.add_argument("--e2e-even-groups", action="store_true",
+                    help="split the end-to-end heads into --e2e-chunks equal groups instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -18,6 +18,22 @@ import torch
 from . import attn
 
 
+def ramped_group_sizes(bh, chunks):
+    """Head-group sizes for `chunks` equal groups shifted by half a group.
+
+    The first and last groups are half as large as the others (32 heads in
+    4 chunks: 4, 8, 8, 8, 4), so the upload before the first forward and the
+    download after the last backward, where nothing else overlaps, are half
+    as long.  Groups of zero heads are dropped; the sizes sum to `bh`.
+    """
+    bh, chunks = int(bh), max(1, int(chunks))
+    if bh < 1:
+        raise ValueError("bh must be >= 1")
+    m = bh / chunks
+    cuts = sorted({0, bh, *(min(bh, int(m / 2 + i * m + 0.5)) for i in range(chunks))})
+    return [b - a for a, b in zip(cuts[:-1], cuts[1:])]
+
+
 class HostAttention:
     """Reusable pipeline for one problem shape (device buffers are reused).
 

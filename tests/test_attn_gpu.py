@@ -271,7 +271,8 @@ def test_stable_forward_caps_the_shift_for_huge_repeated_maxima(A):
 
 @pytest.mark.parametrize("chunks,group_sizes,streams,graph",
                          [(1, None, 1, True), (3, None, 1, True), (3, None, 1, False),
-                          (0, [1, 3, 1], 2, True), (0, [2, 3], 2, False)])
+                          (0, [1, 3, 1], 2, True), (0, [1, 3, 1], 1, True),
+                          (0, [2, 3], 2, False)])
 def test_host_pipeline_matches_device_path(A, chunks, group_sizes, streams, graph):
     """HostAttention (pinned host buffers, head groups pipelined over upload,
     compute and download streams, eagerly or as a replayed CUDA graph) gives
