@@ -180,6 +180,41 @@ def test_matches_torch_fp64_sdpa_with_autograd(causal, n, d):
     np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-11, atol=1e-12)
 
 
+def test_matches_torch_fp64_attention_on_random_small_problems():
+    """Property sweep: random N (including 1), d (including 1), mask, scale and
+    input amplitude (logits up to a few hundred, where an unstabilised softmax
+    overflows); O and the gradients against PyTorch FP64 attention with
+    autograd, LSE against torch.logsumexp of the masked scores."""
+    torch = pytest.importorskip("torch")
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=60, deadline=None, derandomize=True)
+    @hyp.given(n=st.integers(1, 20), d=st.integers(1, 9), causal=st.booleans(),
+               scale=st.floats(0.01, 3.0), amp=st.floats(0.1, 8.0), seed=st.integers(0, 2 ** 16))
+    def check(n, d, causal, scale, amp, seed):
+        q, k, v, do = (amp * _rand(seed + s, n, d) for s in range(4))
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
+            to = torch.nn.functional.scaled_dot_product_attention(
+                tq[None, None], tk[None, None], tv[None, None], is_causal=causal,
+                scale=scale)[0, 0]
+        to.backward(torch.tensor(do))
+        s_t = scale * (torch.tensor(q) @ torch.tensor(k).T)
+        if causal:
+            s_t = s_t.masked_fill(torch.ones(n, n, dtype=torch.bool).triu(1), float("-inf"))
+        o, lse = oracle.forward(q, k, v, scale, causal)
+        dq, dk, dv = oracle.backward(q, k, v, do, scale, causal)
+        tol = dict(rtol=1e-10, atol=1e-10 * (1 + amp ** 3))
+        np.testing.assert_allclose(o, to.detach().numpy(), **tol)
+        np.testing.assert_allclose(lse, torch.logsumexp(s_t, dim=1).numpy(), rtol=1e-12,
+                                   atol=1e-12)
+        for mine, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            np.testing.assert_allclose(mine, ref.numpy(), **tol)
+
+    check()
+
+
 # ---------------------------------------------------------------- finite differences
 
 @pytest.mark.parametrize("causal", [False, True])
