@@ -20,7 +20,10 @@ What it computes, and where that is defined:
   all codes 0.
 
 Pins (tests/test_oracle_int8.py): a hand-derived quantization example with
-ties at .5 (tests/golden/int8_quant_example.txt); codes within [-127, 127]
+ties at .5 (tests/golden/int8_quant_example.txt); a hand-derived forward
+with distinct, non-unit scales on Q and K (tests/golden/
+int8_forward_example.txt: codes, scales, scores, O and LSE), which a
+Q/K scale swap or skipping the quantization fails; codes within [-127, 127]
 with the row maximum at +-127; sign symmetry; the round-trip error bound
 |x - code * s| <= s / 2; exact integer dot products against a pure-Python
 loop; lossless inputs (values already integer multiples of their scale)
@@ -71,15 +74,3 @@ def int8_forward(q, k, v, scale, causal):
     k8, sk = quantize_per_token(k)
     return forward(dequantize(q8, sq), dequantize(k8, sk), v, scale, causal)
 
-
-def int8_forward_bhnd(q, k, v, scale, causal):
-    """int8_forward over the leading [B, H] axes of [B, H, N, d] inputs."""
-    q = np.asarray(q)
-    B, H, N, d = q.shape
-    o = np.empty((B, H, N, d), dtype=np.float64)
-    lse = np.empty((B, H, N), dtype=np.float64)
-    for b in range(B):
-        for h in range(H):
-            o[b, h], lse[b, h] = int8_forward(q[b, h], np.asarray(k)[b, h], np.asarray(v)[b, h],
-                                              scale, causal)
-    return o, lse

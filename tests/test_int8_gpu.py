@@ -164,3 +164,39 @@ def test_int8_as_bf16_rejects_unpadded_scales(A):
     s = torch.zeros(1, 1, 64, dtype=torch.float32, device="cuda")  # [B, H, N], not [B, H, N_pad]
     with pytest.raises(ValueError):
         A.attn_fwd_int8_as_bf16(c, s, c, s, c)
+
+
+def test_both_int8_paths_reproduce_the_hand_derived_forward(A):
+    """tests/golden/int8_forward_example.txt (distinct, non-unit scales on Q and
+    K, two ties at .5) padded with zero columns to d = 64: padding changes no
+    row maximum, no code and no dot product, so codes, scales, O and LSE are
+    the hand-derived ones."""
+    g = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "int8_forward_example.txt")):
+        if line.strip() and not line.startswith("#"):
+            name, r, c, *vals = line.split()
+            g[name] = np.array([float(v) for v in vals]).reshape(int(r), int(c))
+    scale = float(g["scale"][0, 0])
+    t = {}
+    for n in ("q", "k", "v"):
+        x = np.zeros((1, 1, 2, 64), np.float32)
+        x[0, 0, :, :2] = g[n]
+        bits = inputs.f32_to_bf16_bits(x)
+        assert np.array_equal(inputs.bf16_bits_to_f32(bits), x)  # exact in BF16
+        t[n] = _bf16_dev(bits)
+    q8, qs = A.attn_quantize_int8(t["q"])
+    k8, ks = A.attn_quantize_int8(t["k"])
+    assert np.array_equal(q8.cpu().numpy()[0, 0, :, :2], g["q_codes"].astype(np.int8))
+    assert np.array_equal(k8.cpu().numpy()[0, 0, :, :2], g["k_codes"].astype(np.int8))
+    assert np.array_equal(qs.cpu().numpy().reshape(-1), g["q_scale"].reshape(-1))
+    assert np.array_equal(ks.cpu().numpy().reshape(-1), g["k_scale"].reshape(-1))
+    qc, qsp = A.attn_quantize_int8_as_bf16(t["q"])
+    kc, ksp = A.attn_quantize_int8_as_bf16(t["k"])
+    outs = [A.attn_fwd_int8(q8, qs, k8, ks, t["v"], scale=scale, causal=False),
+            A.attn_fwd_int8_as_bf16(qc, qsp, kc, ksp, t["v"], scale=scale, causal=False)]
+    A.attn_check_status()
+    for o, lse in outs:
+        o = o.float().cpu().numpy()[0, 0, :, :2]
+        # BF16 output and BF16 P in P V: within 2^-8 relative of the exact O
+        assert np.all(np.abs(o - g["o"]) <= 2 ** -7 * np.abs(g["o"]) + 1e-6), o
+        assert np.abs(lse.cpu().numpy().reshape(-1) - g["lse"].reshape(-1)).max() <= 1e-5

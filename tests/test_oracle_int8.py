@@ -107,3 +107,52 @@ def test_planted_mistake_fails_the_golden_example():
     safe = np.where(s > 0, s, 1).astype(np.float32)
     away = np.sign(x / safe[:, None]) * np.floor(np.abs(x / safe[:, None]) + 0.5)
     assert not np.array_equal(away.astype(int), codes)
+
+
+# ------------------------------------------------------- worked forward example
+
+FWD_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "int8_forward_example.txt")
+
+
+def _fwd_golden():
+    g = {}
+    for line in open(FWD_GOLDEN):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, rows, cols, *vals = line.split()
+        g[name] = np.array([float(v) for v in vals]).reshape(int(rows), int(cols))
+    g["scale"] = float(g["scale"][0, 0])
+    return g
+
+
+def test_golden_forward_example_codes_scales_scores():
+    g = _fwd_golden()
+    q8, sq = oi.quantize_per_token(g["q"])
+    k8, sk = oi.quantize_per_token(g["k"])
+    assert np.array_equal(q8.astype(int), g["q_codes"].astype(int))
+    assert np.array_equal(k8.astype(int), g["k_codes"].astype(int))
+    assert np.array_equal(sq.astype(np.float64), g["q_scale"].reshape(-1))
+    assert np.array_equal(sk.astype(np.float64), g["k_scale"].reshape(-1))
+    # every score is an exact dyadic rational, so FP64 reproduces it exactly
+    s = oi.int8_scores(q8, sq, k8, sk, g["scale"], False)
+    assert np.array_equal(s, g["s"])
+
+
+def test_golden_forward_example_o_and_lse():
+    g = _fwd_golden()
+    o, lse = oi.int8_forward(g["q"], g["k"], g["v"], g["scale"], False)
+    np.testing.assert_allclose(o, g["o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, g["lse"].reshape(-1), rtol=0, atol=1e-12)
+
+
+def test_planted_scale_swap_and_skipped_quantization_fail_the_forward_example():
+    g = _fwd_golden()
+    q8, sq = oi.quantize_per_token(g["q"])
+    k8, sk = oi.quantize_per_token(g["k"])
+    # slip 1: each tensor's codes paired with the other tensor's scales
+    o_swap, lse_swap = oracle.forward(oi.dequantize(q8, sk), oi.dequantize(k8, sq), g["v"],
+                                      g["scale"], False)
+    assert np.abs(o_swap - g["o"]).max() > 1.0 and np.abs(lse_swap - g["lse"]).max() > 1.0
+    # slip 2: no quantization at all
+    o_raw, lse_raw = oracle.forward(g["q"], g["k"], g["v"], g["scale"], False)
+    assert np.abs(o_raw - g["o"]).max() > 1e-2 and np.abs(lse_raw - g["lse"]).max() > 1e-3
