@@ -91,15 +91,19 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  * Forward pass with the stabilised normaliser of "Why Low-Precision Transformer
  * Training Fails" (Figure 7 and Algorithm 1): while a row's running maximum
  * r_m of scale * q.k is attained by two or more keys, the exponentials are
- * taken relative to m = beta * r_m if r_m > 0 and m = 0 if r_m < 0 (r_m = 0:
- * m = r_m), so that no unnormalised probability exp(S - m) is exactly 1.
- * Mathematically O and LSE are those of attn_fwd (LSE is formed with the
- * normaliser actually used); only the rounding differs.  attn_bwd accepts
- * its outputs unchanged.  BF16 only; beta must be finite and > 1.  The shift
- * is capped so that the row's largest exponent stays at or above 2^-64: for
- * very large repeated maxima ((beta - 1) * scale * r_m * log2(e) > 64) the
- * normaliser is r_m + 64 / (scale * log2(e)) instead of beta * r_m, which
- * keeps every exponential below 1 without underflowing the whole row.
+ * taken relative to m = beta * r_m if r_m > 0 and m = 0 if r_m <= 0, so that
+ * no unnormalised probability exp(S - m) is exactly 1.  Mathematically O and
+ * LSE are those of attn_fwd (LSE is formed with the normaliser actually
+ * used); only the rounding differs.  attn_bwd accepts its outputs unchanged.
+ * BF16 only; beta must be finite and > 1.  With c = scale * log2(e), m is
+ * then kept within [r_m + 2^-8 / c, r_m + 64 / c]:
+ *   - the floor makes the row's largest exponent "sufficiently negative" (the
+ *     paper's words) once rounded: 2^(c (r_m - m)) <= 2^(-2^-8) rounds to at
+ *     most 1 - 2^-8 in BF16, also for repeated maxima that are 0, tiny, or
+ *     tiny and negative, where beta * r_m or 0 alone would leave the BF16
+ *     operand of the P V product at exactly 1;
+ *   - the cap keeps the largest exponential at or above 2^-64, so a very
+ *     large repeated maximum cannot underflow the whole row.
  */
 ATTN_API attn_status attn_fwd_stable(const void* q, const void* k, const void* v, void* o,
                                      float* lse, int B, int H, int N, int d, float scale,
@@ -224,6 +228,14 @@ ATTN_API attn_status attn_bwd_dq_convert(void* dq, int B, int H, int N, int d, f
  * of the library on the current device.  Returns ATTN_ERR_TIMEOUT if any
  * kernel gave up on a bounded wait since the last check, ATTN_ERR_CUDA if
  * the stream reports an error, else ATTN_OK.
+ *
+ * The status words are per device and per process, not per stream or per
+ * call: a timeout recorded by any of this library's kernels on the current
+ * device, launched from any stream or host thread, is reported by the next
+ * attn_check_status on that device, whatever stream it is given, and that
+ * check clears it.  `stream` only selects what is synchronized first; a
+ * caller that needs to attribute a timeout to one call must check after that
+ * call with no other call of the library in flight on the device.
  */
 ATTN_API attn_status attn_check_status(cudaStream_t stream);
 
@@ -254,7 +266,11 @@ ATTN_API attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, cud
  *     streams, unordered host threads) race and give wrong results.  Each call
  *     rewrites what it reads (the dQ accumulator is zeroed every call).
  *   - The first call on a device looks up the array's device address; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The address is kept with
+ *     the id of the CUDA context it belongs to; after cudaDeviceReset the next
+ *     call looks it up again, so that call too belongs before any capture.
+ *   - Shape errors are those of attn_bwd (ATTN_ERR_UNSUPPORTED for a head size
+ *     outside {64, 128}, ATTN_ERR_INVALID_ARG for a bad N, B*H or scale).
  */
 ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                       const float* lse, const void* dout, void* dq, void* dk,

@@ -2,7 +2,9 @@
 
 Each .cu file under csrc/ is compiled in parallel to an object under
 _build/, then linked into precision_numerics_gb300/_lib/libattn.so with the
-CUDA runtime linked statically.  A rebuild happens when any source or
+CUDA runtime linked statically.  build_test_variant() makes the test build
+(_lib/libattn_testhooks.so, objects under _build_testhooks/), which only the
+test suite loads.  A rebuild happens when any source or
 header is newer than the library.
 """
 from __future__ import annotations
@@ -43,23 +45,37 @@ def _inputs():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+# The test build: the same sources with test-only instrumentation compiled in
+# (ATTN_TEST_HOOKS: counters and a stall switch in the forward kernel) and a
+# 50 ms limit on every in-kernel wait.  Only the test suite loads it.
+TEST_VARIANT = "testhooks"
+TEST_FLAGS = ("-DATTN_TEST_HOOKS", "-DATTN_TEST_WAIT_LIMIT_NS=50000000ull")
+
+
+def lib_path(variant: str = "") -> str:
+    return LIB if not variant else os.path.join(LIB_DIR, f"libattn_{variant}.so")
+
+
+def needs_build(variant: str = "") -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libattn.so; returns its path."""
-    if not force and not needs_build():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
+    """Compile and link libattn.so (or libattn_<variant>.so); returns its path."""
+    lib = lib_path(variant)
+    if not force and not needs_build(variant):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if not variant else BUILD + "_" + variant
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -71,13 +87,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libattn.so failed:\n{r.stderr}\n{r.stdout}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stderr}\n{r.stdout}")
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_test_variant(force: bool = False) -> str:
+    """The test build (TEST_FLAGS) as _lib/libattn_testhooks.so; returns its path."""
+    return build(force=force, extra_flags=TEST_FLAGS, variant=TEST_VARIANT)
 
 
 if __name__ == "__main__":

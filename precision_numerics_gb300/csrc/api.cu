@@ -35,6 +35,8 @@ attn_status cuda_fail(cudaError_t err, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+}  // namespace
+
 // Shape and scalar checks shared by every entry point.
 attn_status check_problem(int B, int H, int N, int d, attn_dtype dt, float scale, bool need_scale,
                           Problem* out) {
@@ -60,6 +62,8 @@ attn_status check_problem(int B, int H, int N, int d, attn_dtype dt, float scale
   out->causal = 0;
   return ATTN_OK;
 }
+
+namespace {
 
 // Pointer must be non-null, 16-byte aligned and reachable from the current
 // device (device memory of this device, or managed memory).

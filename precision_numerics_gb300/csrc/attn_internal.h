@@ -98,6 +98,11 @@ cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream);
 cudaError_t read_and_clear_status_bwd(unsigned int* out, cudaStream_t stream);
 cudaError_t read_and_clear_status_misc(unsigned int* out, cudaStream_t stream);
 
+// Shape and scalar checks shared by every entry point (d, N, B*H*N*d, dtype,
+// and the scale when need_scale); fills *out and records the error detail.
+attn_status check_problem(int B, int H, int N, int d, attn_dtype dt, float scale, bool need_scale,
+                          Problem* out);
+
 // Record the detail text returned by attn_last_error() on this thread.
 void set_last_error(const char* msg);
 

@@ -23,7 +23,11 @@
 //    accumulator.
 //  * The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress while that device is current; make that first call
-//    before any stream capture.  No call allocates memory.
+//    before any stream capture.  The address is cached together with the
+//    unique id of the CUDA context it belongs to: after cudaDeviceReset (a new
+//    primary context, in which the module and the array are loaded afresh) the
+//    next call looks the address up again, so that first call after a reset
+//    should also come before any stream capture.  No call allocates memory.
 #include <mutex>
 #include <stdio.h>
 
@@ -39,11 +43,40 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_bwd_scratch[kBwdScratchBytes];
 
 std::mutex g_setup_mutex;
+// Per device: the array's device address and the id of the context it is valid in.
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
 attn_status noalloc_fail(attn_status s, const char* msg) {
   set_last_error(msg);
   return s;
+}
+
+// Unique id of the calling thread's current CUDA context (driver entry
+// points resolved once, no -lcuda); false when there is none or the driver
+// lacks the calls.
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -58,11 +91,13 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
                              int B, int H, int N, int d, float scale, int causal,
                              cudaStream_t stream) {
-  // Shape and size checks first: nothing is launched for a rejected call.
-  const size_t need = attn_bwd_workspace_bytes(B, H, N, d, ATTN_DTYPE_BF16);
-  if (need == 0)
-    return noalloc_fail(ATTN_ERR_INVALID_ARG,
-                        "attn_bwd_noalloc: invalid shape (see attn_bwd_workspace_bytes)");
+  // Shape and size checks first: nothing is launched for a rejected call.  The
+  // shape check is attn_bwd's own, so both entry points report the same status
+  // (ATTN_ERR_UNSUPPORTED for a head size outside {64, 128}, for instance).
+  Problem p;
+  const attn_status shape = check_problem(B, H, N, d, ATTN_DTYPE_BF16, scale, true, &p);
+  if (shape != ATTN_OK) return shape;
+  const size_t need = bwd_workspace_bytes(p);
   if (need > kBwdScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
@@ -77,18 +112,22 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
+    if (g_scratch_ptr[dev] == nullptr || !have_ctx || g_scratch_ctx[dev] != ctx) {
       // Host code must not use g_bwd_scratch directly (that is a host-side
-      // stand-in); ask the runtime for the device address on this device.
-      void* p = nullptr;
-      cudaError_t err = cudaGetSymbolAddress(&p, g_bwd_scratch);
-      if (err != cudaSuccess || p == nullptr) {
+      // stand-in); ask the runtime for the device address in the current
+      // context (this also sets the context up if no call has yet).
+      void* addr = nullptr;
+      cudaError_t err = cudaGetSymbolAddress(&addr, g_bwd_scratch);
+      if (err != cudaSuccess || addr == nullptr) {
         char msg[256];
         snprintf(msg, sizeof(msg), "attn_bwd_noalloc: cudaGetSymbolAddress failed: %s",
                  cudaGetErrorString(err));
         return noalloc_fail(ATTN_ERR_CUDA, msg);
       }
-      g_scratch_ptr[dev] = p;
+      g_scratch_ptr[dev] = addr;
+      g_scratch_ctx[dev] = current_context_id(&ctx) ? ctx : 0;
     }
     scratch = g_scratch_ptr[dev];
   }

@@ -97,6 +97,20 @@ struct FwdCfg {
 
 __device__ __forceinline__ void set_fail(unsigned int code) { atomicOr(&g_status_fwd, code); }
 
+#ifdef ATTN_TEST_HOOKS
+// Test instrumentation, compiled only into the separate test build of the
+// library (ATTN_TEST_HOOKS), never into libattn.so:
+//  - g_hook_pbar_ones: when set, every query row adds the number of its BF16
+//    P-bar operands (the P V inputs) equal to exactly 1.0 into
+//    g_hook_pbar_ones[b*H*N + h*N + row] (rows below g_hook_rows only);
+//  - g_hook_stall: when set, the first softmax warpgroup of CTA 0 first waits
+//    on a barrier that nothing ever arrives at, so the wait runs out (after the
+//    test build's short limit) and the kernel takes its failure path.
+static __device__ unsigned int* g_hook_pbar_ones;
+static __device__ unsigned long long g_hook_rows;
+static __device__ int g_hook_stall;
+#endif
+
 // Number of K/V tiles the query tile starting at row q_first visits.
 __device__ __forceinline__ int kv_tiles_for(int q_first, int N, bool causal) {
   if (q_first >= N) return 0;
@@ -191,6 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int k = 0; k < C::kKsSlots; ++k) mbar_init(&bar_ksfull[k], 1);
     mbar_init(bar_final, 1);
+#ifdef ATTN_TEST_HOOKS
+    mbar_init(reinterpret_cast<uint64_t*>(tmem_slot + 2), 1);  // nothing arrives here
+#endif
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -470,6 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // previous tiles used (equal to m_run except in the stabilised variant).
       float m_run = -INFINITY, m_norm = -INFINITY, l_run = 0.f;
       int n_at_max = 0;  // stabilised variant: elements equal to m_run so far (saturates at 2)
+#ifdef ATTN_TEST_HOOKS
+      unsigned int n_ones = 0;  // BF16 P-bar operands equal to 1.0 in this row
+      if (g_hook_stall && blockIdx.x == 0 && t == 0 && rr == 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(reinterpret_cast<uint64_t*>(tmem_slot + 2), 0));
+        if (!ok) break;
+      }
+#endif
       for (int j = 0; j < n; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_sfull[t], (sc + j) & 1));
         if (!ok) break;
@@ -541,8 +565,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 128; ++c) cnt += __uint_as_float(s[c >> 5][c & 31]) == tile_max;
             n_at_max = min(2, (tile_max > m_run ? 0 : n_at_max) + cnt);
           }
-          if (n_at_max >= 2) {
-            m_use = m_new > 0.f ? beta * m_new : (m_new < 0.f ? 0.f : m_new);
+          if (n_at_max >= 2 && m_new != -INFINITY) {
+            m_use = m_new > 0.f ? beta * m_new : 0.f;
+            // "Sufficiently negative": the row's largest exponent c * (r_m - m)
+            // (base 2) is at most -2^-8, so its P-bar = 2^(c (r_m - m)) <= 0.99730
+            // rounds to at most 1 - 2^-8 in BF16.  Without this floor a small
+            // repeated maximum (0 <= c (beta - 1) r_m < 2.8e-3, r_m = 0, or
+            // -2.8e-3 < c r_m < 0) still gives P-bar operands equal to 1.
+            m_use = fmaxf(m_use, m_new + 0.00390625f / scale_log2);
             // Keep the row's largest exponent c * (r_m - m) at or above -64 (base 2),
             // so a very large repeated maximum cannot underflow every exponential
             // of the row (the pages do not discuss that range).
@@ -574,6 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = ex2(x1);
             sums2[i & 3] = add2(sums2[i & 3], f2_pack(p0, p1));
             pk[i] = pack_bf16x2(p0, p1);
+#ifdef ATTN_TEST_HOOKS
+            n_ones += ((pk[i] & 0xFFFFu) == 0x3F80u) + ((pk[i] >> 16) == 0x3F80u);
+#endif
           }
           tmem_st16(tS + c * 16, pk);
         }
@@ -660,6 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (qi < N) lse[(size_t)it.bh * N + qi] = m_norm * (I8 ? scale * sq : scale) + logf(l_run);
+#ifdef ATTN_TEST_HOOKS
+      if (qi < N && g_hook_pbar_ones != nullptr && (size_t)it.bh * N + qi < g_hook_rows)
+        atomicAdd(g_hook_pbar_ones + (size_t)it.bh * N + qi, n_ones);
+#endif
     }
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
   }
@@ -734,6 +771,18 @@ cudaError_t launch_fwd_int8_as_bf16(const Problem& p, const void* qc, const floa
   return p.causal ? launch_fwd_impl<64, true, false, true>(p, mq, mk, mv, mo, o, lse, 0.f, stream, qs, ks)
                   : launch_fwd_impl<64, false, false, true>(p, mq, mk, mv, mo, o, lse, 0.f, stream, qs, ks);
 }
+
+#ifdef ATTN_TEST_HOOKS
+extern "C" ATTN_API int attn_testhook_pbar_counter(unsigned int* counts, unsigned long long rows) {
+  cudaError_t e = cudaMemcpyToSymbol(g_hook_pbar_ones, &counts, sizeof(counts));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_hook_rows, &rows, sizeof(rows));
+  return (int)e;
+}
+
+extern "C" ATTN_API int attn_testhook_stall(int on) {
+  return (int)cudaMemcpyToSymbol(g_hook_stall, &on, sizeof(on));
+}
+#endif
 
 cudaError_t read_and_clear_status_fwd(unsigned int* out, cudaStream_t stream) {
   static const unsigned int zero = 0;

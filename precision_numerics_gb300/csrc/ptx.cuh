@@ -15,7 +15,13 @@ namespace attn {
 // kernel then records a code in a per-translation-unit status word (read back
 // by attn_check_status) and winds down instead of hanging.
 // ---------------------------------------------------------------------------
+#ifdef ATTN_TEST_WAIT_LIMIT_NS
+// Test build of the library only: a shorter limit, so that a wait made to run
+// out by a test hook ends the kernel quickly.
+constexpr unsigned long long kWaitLimitNs = ATTN_TEST_WAIT_LIMIT_NS;
+#else
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+#endif
 constexpr uint32_t kWaitSpinCap = 1u << 30;                  // hard cap on polls
 
 __device__ __forceinline__ uint64_t globaltimer() {

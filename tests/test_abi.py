@@ -136,3 +136,24 @@ def test_int8_entry_points_check_arguments_before_any_launch(lib):
 
 def test_int8_padded_scale_rows():
     assert [attn.int8_scale_rows(n) for n in (1, 127, 128, 129, 4096)] == [128, 128, 128, 256, 4096]
+
+
+def test_status_check_is_per_device_not_per_stream(lib):
+    """attn_check_status takes only a stream (no workspace): the header states that
+    its status words are shared by every stream and thread on the device."""
+    assert attn._SIGNATURES["attn_check_status"][1] == [ctypes.c_void_p]
+    text = open(HEADER).read()
+    block = text[text.index("ATTN_API attn_status attn_check_status") - 1200:
+                 text.index("ATTN_API attn_status attn_check_status")]
+    assert "per device and per process, not per stream" in block
+
+
+def test_noalloc_backward_reports_the_same_shape_errors_as_attn_bwd(lib):
+    f = ctypes.c_float
+    for d, want in ((96, attn.ATTN_ERR_UNSUPPORTED), (64, attn.ATTN_ERR_INVALID_ARG)):
+        n = 128 if d == 96 else 0  # d = 96: unsupported head size; N = 0: invalid
+        r_noalloc = lib.attn_bwd_noalloc(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, n, d, f(0.125),
+                                         1, None)
+        r_bwd = lib.attn_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, n, d, f(0.125), 1, 0, 16,
+                             1 << 20, None)
+        assert r_noalloc == r_bwd == want, (d, r_noalloc, r_bwd)

@@ -208,6 +208,20 @@ def test_bounded_wait_reports_timeout_and_context_survives(A):
     _assert_bf16(got, _oracle(x, "bf16", 0.125, False, backward=False), backward=False)
 
 
+def test_timeout_status_is_shared_by_all_streams(A):
+    """The status words are per device, not per stream (include/attn.h at
+    attn_check_status): a timeout recorded by a kernel on one stream is
+    reported by a check on another stream, and that check clears it."""
+    A.attn_check_status()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    A.attn_selftest_wait_timeout(1_000_000, stream=s1)
+    s1.synchronize()
+    with pytest.raises(A.AttnError) as info:
+        A.attn_check_status(stream=s2)
+    assert info.value.status == A.ATTN_ERR_TIMEOUT
+    A.attn_check_status(stream=s1)  # already cleared by the check on s2
+
+
 def test_rejects_host_memory(A):
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device="cuda")
     lib = A.load_library()

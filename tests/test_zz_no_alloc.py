@@ -77,3 +77,21 @@ def test_rejects_problems_beyond_the_fixed_scratch(lib):
     assert status == 1  # ATTN_ERR_INVALID_ARG, before anything is launched
     msg = lib.attn_last_error().decode()
     assert "33554432" in msg and "attn_bwd" in msg
+
+
+def test_python_binding_at_the_largest_listed_problem(lib):
+    """attn.attn_bwd_noalloc (the binding's checks and default scale) on B8 H12
+    N1024 d64 causal, the size the header names as fitting the fixed array
+    (25.9 MB of its 32 MiB), against attn_bwd with its own workspace."""
+    from precision_numerics_gb300 import attn
+    t = _problem(13, 8, 12, 1024, 64)
+    o, lse = attn.attn_fwd(t["q"], t["k"], t["v"], causal=True)
+    ref = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=True)
+    assert attn.attn_bwd_workspace_bytes(8, 12, 1024, 64) <= 32 << 20
+    got = [torch.full_like(o, float("nan")) for _ in range(3)]
+    attn.attn_bwd_noalloc(t["q"], t["k"], t["v"], o, lse, t["do"], *got, causal=True)
+    attn.attn_check_status()
+    for name, r, g in zip(("dq", "dk", "dv"), ref, got):
+        assert bool(torch.isfinite(g.float()).all()), name
+        assert _rel_l2(g, r) <= 1e-2, (name, _rel_l2(g, r))
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
