@@ -250,6 +250,45 @@ def run_reference(args, w, budget_s=150.0):
     return 0
 
 
+def _kernel_delta(ws, w, head):
+    """delta of one (b, h) head as the preprocess kernel wrote it into the
+    backward workspace (layout in include/attn.h: -LSE*log2(e) [B*H][N_pad],
+    then delta [B*H][N_pad] from the next 256-byte boundary)."""
+    n_pad = (w.N + 127) // 128 * 128
+    rows = w.B * w.H * n_pad
+    off = (rows * 4 + 255) // 256 * 256 + head * n_pad * 4
+    return ws[off:off + w.N * 4].cpu().numpy().view(np.float32).astype(np.float64)
+
+
+def _dev3(d):
+    return {k: d[k] for k in ("max_abs", "mean_abs", "signed_mean")}
+
+
+def _deviation_block(w, f, o, dv, ws, o_ref, dv_ref, head=0):
+    """Tiled GPU vs FP64 next to naive BF16 attention vs FP64 on one head: the
+    question of "Is Flash Attention Stable?" (abstract) -- how much more
+    numeric deviation tiled attention has than Baseline Attention at BF16 --
+    answered on this workload.  delta_lp is the backward kernel's own delta
+    (rowsum(dO o O) from the stored BF16 O, "Why Low-Precision Transformer
+    Training Fails", Figure 3) against rowsum(dO o O) of the exact O.
+    f: the head's inputs (FP32 arrays); o_ref, dv_ref: the oracle's O and dV."""
+    import oracle
+    from precision_numerics_gb300.deviation import deviation
+    B, H, N, d = w.B, w.H, w.N, w.d
+    o_nv, _ = oracle.naive_bf16_forward(f["q"], f["k"], f["v"], w.scale, w.causal)
+    dv_nv = oracle.naive_bf16_backward(f["q"], f["k"], f["v"], f["do"], w.scale, w.causal)[2]
+    tiled = {"o": deviation(o.reshape(B * H, N, d)[head].float().cpu().numpy(), o_ref),
+             "dv": deviation(dv.reshape(B * H, N, d)[head].float().cpu().numpy(), dv_ref)}
+    naive = {"o": deviation(o_nv, o_ref), "dv": deviation(dv_nv, dv_ref)}
+    dl = deviation(_kernel_delta(ws, w, head), oracle.delta(f["do"], o_ref))
+    return {"sample": f"head (b,h)=(0,{head}) of the timed workload against the FP64 definition",
+            "tiled_gpu": {k: _dev3(v) for k, v in tiled.items()},
+            "naive_bf16": {k: _dev3(v) for k, v in naive.items()},
+            "naive_over_tiled_o_max_abs": naive["o"]["max_abs"] / tiled["o"]["max_abs"],
+            "naive_over_tiled_o_mean_abs": naive["o"]["mean_abs"] / tiled["o"]["mean_abs"],
+            "delta_lp_minus_delta": _dev3(dl)}
+
+
 def _config(w):
     return {"workload": f"{w.name}: B{w.B} H{w.H} N{w.N} d{w.d} "
                         f"{'causal' if w.causal else 'non-causal'} BF16 forward+backward",
@@ -396,6 +435,8 @@ def run_ours(args, w):
             "clocks": sampler.summary(),
         }
         line["fwd_tflops"] = _fwd_only_tflops(attn, t, o, lse, w, stream, torch)
+        line["deviation"] = _deviation_block(w, f, o, dv, ws, o_ref, g_ref[2])
+        line["host_us_per_call"] = _host_cost(attn, w, dev, torch)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, x)
         print(json.dumps(line), flush=True)
@@ -403,6 +444,57 @@ def run_ours(args, w):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def _host_cost(attn, w, dev, torch, calls=200):
+    """Host time per eager call of attn_fwd + attn_bwd, in microseconds.
+
+    "c_abi": the two C entry points called through ctypes with prepared
+    arguments (the library's own host cost: argument and pointer checks,
+    tensor-map encoding, launches); "python": the same through the Python
+    binding (plus its checks and marshalling).  Measured on the small
+    forward-only workload's shape with a backward (B1 H2 N128 d64) and on this
+    workload's shape, after the timed region; the GPU work of a call is
+    shorter than its host time on the small shape, so calls do not queue."""
+    import ctypes
+    lib = attn.load_library()
+    out = {}
+    for tag, (B, H, N, d) in (("B1H2N128d64", (1, 2, 128, 64)),
+                              (f"B{w.B}H{w.H}N{w.N}d{w.d}", (w.B, w.H, w.N, w.d))):
+        z = {k: torch.zeros((B, H, N, d), dtype=torch.bfloat16, device=dev)
+             for k in ("q", "k", "v", "o", "do", "dq", "dk", "dv")}
+        lse = torch.zeros((B, H, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(attn.attn_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+        st = torch.cuda.current_stream().cuda_stream
+        sc = ctypes.c_float(d ** -0.5)
+        fa = (z["q"].data_ptr(), z["k"].data_ptr(), z["v"].data_ptr(), z["o"].data_ptr(),
+              lse.data_ptr(), B, H, N, d, sc, 1, 0, st)
+        ba = (z["q"].data_ptr(), z["k"].data_ptr(), z["v"].data_ptr(), z["o"].data_ptr(),
+              lse.data_ptr(), z["do"].data_ptr(), z["dq"].data_ptr(), z["dk"].data_ptr(),
+              z["dv"].data_ptr(), B, H, N, d, sc, 1, 0, ws.data_ptr(), ws.numel(), st)
+        n = calls if N <= 1024 else 20
+
+        def c_abi():
+            assert lib.attn_fwd(*fa) == 0 and lib.attn_bwd(*ba) == 0
+
+        def python():
+            attn.attn_fwd(z["q"], z["k"], z["v"], causal=True, o=z["o"], lse=lse)
+            attn.attn_bwd(z["q"], z["k"], z["v"], z["o"], lse, z["do"], causal=True, dq=z["dq"],
+                          dk=z["dk"], dv=z["dv"], workspace=ws)
+
+        res = {}
+        for name, fn in (("c_abi", c_abi), ("python", python)):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(n):
+                fn()
+            res[name] = (time.perf_counter() - t0) / n * 1e6
+            torch.cuda.synchronize()
+        attn.attn_check_status()
+        out[tag] = res
+    return out
 
 
 def _fwd_only_tflops(attn, t, o, lse, w, stream, torch, reps=20):
@@ -427,9 +519,10 @@ def run_deviation(args):
     For O, LSE, dQ, dK, dV: the tiled GPU kernel, the tiled GPU kernel with
     the stabilised normaliser (beta = 2; on the exact-tie workload also beta =
     1.05, 1.5 and 4), and the naive BF16 attention, each against the FP64
-    definition; for O and LSE also the INT8-input forward.  Also delta = rowsum(dO o O) formed from the
-    GPU's BF16 O (delta_lp, what the backward uses) against delta from the
-    exact O ("Why Low-Precision Transformer Training Fails", Figure 3).
+    definition; for O and LSE also the INT8-input forward.  Also delta_lp, the
+    rowsum(dO o O) that the backward's preprocess kernel formed from the GPU's
+    BF16 O (read back from its workspace), against delta from the exact O
+    ("Why Low-Precision Transformer Training Fails", Figure 3).
     """
     import torch
 
@@ -455,9 +548,13 @@ def run_deviation(args):
                                  lambda *a, _b=beta, **kw: attn.attn_fwd_stable(*a, beta=_b, **kw)))
         for tag, fwd in variants:
             o, lse = fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
-            g = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale, causal=w.causal)
+            ws = torch.empty(attn.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.d),
+                             dtype=torch.uint8, device="cuda")
+            g = attn.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale,
+                              causal=w.causal, workspace=ws)
             attn.attn_check_status()
-            runs[tag] = {"o": o, "lse": lse, "dq": g[0], "dk": g[1], "dv": g[2]}
+            runs[tag] = {"o": o, "lse": lse, "dq": g[0], "dk": g[1], "dv": g[2],
+                         "delta": _kernel_delta(ws, w, 0)}
         head = 0
         f = {k: inputs.bf16_bits_to_f32(v.reshape(w.B * w.H, w.N, w.d)[head]) for k, v in x.items()}
         o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], w.scale, w.causal)
@@ -472,8 +569,8 @@ def run_deviation(args):
             for k in ref:
                 gv = r[k].reshape(w.B * w.H, *r[k].shape[2:])[head].float().cpu().numpy()
                 rep[tag][k] = deviation(gv, ref[k])
-            o_lp = r["o"].reshape(w.B * w.H, w.N, w.d)[head].float().cpu().numpy()
-            rep[tag]["delta"] = deviation(oracle.delta(f["do"], o_lp), oracle.delta(f["do"], o_ref))
+            # delta_lp as the backward's preprocess kernel computed it
+            rep[tag]["delta"] = deviation(r["delta"], oracle.delta(f["do"], o_ref))
         for k in ref:
             rep["naive_bf16"][k] = deviation(naive[k], ref[k])
         # INT8-input forward (per-token INT8 Q and K, BF16 V): O and LSE only
