@@ -608,27 +608,34 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 // ---------------------------------------------------------------------------
 // 2'. main kernel, persistent variant (used for d = 64)
 // ---------------------------------------------------------------------------
-// The pipeline above, in CTAs that stay resident: each CTA walks a static
-// list of (b, h, j) items (heaviest first, dealt in snake order), with the
-// barrier phases counted across items.  An item's first Q / dO tile loads
-// while the previous item finishes; its K_j / V_j load once the previous
-// item's products have completed; its first S^T and dP^T products are issued
-// while the compute warps still write the previous item's dV and dK, which
-// warp 3 stores with TMA from two staging slots.
-// Persistent variant (d = 64): the shared-memory layout of Cfg plus one
-// staging slot each for dV and dK (a 64-column chunk, 128 rows x 128 bytes):
-// the Q / dO rings already hold the next item's tiles during an epilogue.
-// kv_full, q_full[3], q_empty[3], s_full[2], p_ready[2], dp_full, ds_ready,
-// dq_full, dq_free, dq_done[2], item_done, mma_final, epi_full[2], epi_free[2]
-constexpr int kNumBarsP = 1 + 3 + 3 + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 1 + 1 + 2 + 2;
+// The five products of the kernel above, in CTAs that stay resident: each CTA
+// walks a static list of (b, h, j) items (heaviest first, dealt in snake
+// order), with the barrier phases counted across items.  At d = 64 the
+// products of a 64-row tile take ~900 cycles while the P and dS work of the
+// compute warps takes longer, so this variant spends the TMEM and shared
+// memory that d = 64 leaves free on taking waits off the compute warps' chain:
+//   - dP^T is double-buffered and issued two tiles ahead (with S^T), so the
+//     dS of a tile never waits for the dK product of the previous tile;
+//   - dQ^T is double-buffered, so the dQ^T product never waits for the drain
+//     warps to have read the previous one;
+//   - K_j and V_j are double-buffered, so the next item's K and V load while
+//     the current item runs, and its first products follow the current
+//     item's last ones without a load in between.
+// Per 64-row tile T (b = T % 2) the MMA warp issues dV(T), dK(T), dQ^T(T) into
+// dQ buffer b, then S^T(T+2) and dP^T(T+2) into S and dP buffers b.  dV and dK
+// are staged 64 columns at a time and stored by warp 3 with TMA.
+// kv_full[2], kv_free[2], q_full[3], q_empty[3], s_full[2], p_ready[2],
+// dp_full[2], ds_ready, dq_full[2], dq_free[2], dq_done[2], item_done,
+// mma_final, epi_full[2], epi_free[2]
+constexpr int kNumBarsP = 2 + 2 + 3 + 3 + 2 + 2 + 2 + 1 + 2 + 2 + 2 + 1 + 1 + 2 + 2;
 template <int D>
 struct PCfg {
-  static constexpr int kChunks = D / 64;          // 64-column (128-byte) chunks per row
-  static constexpr int kKVBytes = 128 * D * 2;    // K_j or V_j (128 rows x d)
+  static_assert(D == 64, "the persistent variant is laid out for d = 64");
+  static constexpr int kKVBytes = 128 * D * 2;    // K_j or V_j (128 rows x d), one chunk
   static constexpr int kQBytes = kBM * D * 2;     // Q_i or dO_i (64 rows x d)
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kKVBytes;
-  static constexpr int kOffQ = kOffV + kKVBytes;
+  static constexpr int kOffK = 0;                 // two K slots
+  static constexpr int kOffV = kOffK + 2 * kKVBytes;  // two V slots
+  static constexpr int kOffQ = kOffV + 2 * kKVBytes;
   static constexpr int kOffDO = kOffQ + kStages * kQBytes;
   static constexpr int kOffDS = kOffDO + kStages * kQBytes;
   static constexpr int kOffStage = kOffDS + 2 * kDSBytes;
@@ -636,9 +643,10 @@ struct PCfg {
   static constexpr int kOffDelta = kOffLse + kStages * kBM * 4;
   static constexpr int kOffBar = kOffDelta + kStages * kBM * 4;
   static constexpr int kSmemBytes = kOffBar + kNumBarsP * 8 + 16;
-  static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128,
-                            kColDQ = 2 * D + 192;
-  static_assert(kColDQ + kBM <= 512, "TMEM columns");
+  // TMEM: dV, dK (64 each), S^T, dP^T and dQ^T double-buffered (64 each).
+  static constexpr uint32_t kColDV = 0, kColDK = 64, kColS = 128, kColDP = 256, kColDQ = 384;
+  static_assert(kColDQ + 2 * kBM <= 512, "TMEM columns");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 // Work item L of the main kernel: head bh, key tile j, and its query tiles.
@@ -691,20 +699,21 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   auto item = [&](int L) { return bwd_item(L, BH, n_kt, n_qt, heads_per_group, CAUSAL); };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* bar_kv = bars + 0;
-  uint64_t* bar_qfull = bars + 1;    // [3]
-  uint64_t* bar_qempty = bars + 4;   // [3]
-  uint64_t* bar_sfull = bars + 7;    // [2]
-  uint64_t* bar_pready = bars + 9;   // [2]
-  uint64_t* bar_dpfull = bars + 11;
-  uint64_t* bar_dsready = bars + 12;
-  uint64_t* bar_dqfull = bars + 13;
-  uint64_t* bar_dqfree = bars + 14;
-  uint64_t* bar_dqdone = bars + 15;  // [2]
-  uint64_t* bar_itemdone = bars + 17;  // every product of an item has completed
-  uint64_t* bar_final = bars + 18;
-  uint64_t* bar_epifull = bars + 19;   // [2] a staged dV / dK chunk is complete
-  uint64_t* bar_epifree = bars + 21;   // [2] its TMA store has read the staging slot
+  uint64_t* bar_kvfull = bars + 0;     // [2] K_j / V_j slot loaded
+  uint64_t* bar_kvfree = bars + 2;     // [2] every product reading the slot has completed
+  uint64_t* bar_qfull = bars + 4;      // [3]
+  uint64_t* bar_qempty = bars + 7;     // [3]
+  uint64_t* bar_sfull = bars + 10;     // [2]
+  uint64_t* bar_pready = bars + 12;    // [2]
+  uint64_t* bar_dpfull = bars + 14;    // [2]
+  uint64_t* bar_dsready = bars + 16;
+  uint64_t* bar_dqfull = bars + 17;    // [2]
+  uint64_t* bar_dqfree = bars + 19;    // [2]
+  uint64_t* bar_dqdone = bars + 21;    // [2]
+  uint64_t* bar_itemdone = bars + 23;  // every product of an item has completed
+  uint64_t* bar_final = bars + 24;
+  uint64_t* bar_epifull = bars + 25;   // [2] a staged dV / dK chunk is complete
+  uint64_t* bar_epifree = bars + 27;   // [2] its TMA store has read the staging slot
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarsP);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -712,22 +721,23 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
     *s_abort = (smem_u32(smem) & 1023u) != 0;
-    mbar_init(bar_kv, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_qfull[s], 1);
       mbar_init(&bar_qempty[s], 1 + 8);  // MMA commit + one arrive per compute warp
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_kvfull[b], 1);
+      mbar_init(&bar_kvfree[b], 1);
       mbar_init(&bar_sfull[b], 1);
       mbar_init(&bar_pready[b], 256);
+      mbar_init(&bar_dpfull[b], 1);
+      mbar_init(&bar_dqfull[b], 1);
+      mbar_init(&bar_dqfree[b], 128);
       mbar_init(&bar_dqdone[b], 1);
       mbar_init(&bar_epifull[b], 128);
       mbar_init(&bar_epifree[b], 1);
     }
-    mbar_init(bar_dpfull, 1);
     mbar_init(bar_dsready, 256);
-    mbar_init(bar_dqfull, 1);
-    mbar_init(bar_dqfree, 128);
     mbar_init(bar_itemdone, 1);
     mbar_init(bar_final, 1);
     fence_mbar_init();
@@ -755,10 +765,12 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   float* sDelta = reinterpret_cast<float*>(smem + C::kOffDelta);
 
   // Barrier phases run on across items.  Every role numbers the 64-row query
-  // tiles it has handled in this CTA (T); the Q / dO ring slot is T % 3, the
-  // S^T buffer T % 2, and the per-tile barriers complete once per T.  Items
-  // with no query tile (none occur for the shapes accepted) are skipped by
-  // every role alike.
+  // tiles it has handled in this CTA (T) and the items (n); the Q / dO ring
+  // slot is T % 3, the S^T, dP^T and dQ^T buffers T % 2, the K / V slot n % 2.
+  // A barrier of a double buffer completes once per use of its buffer, and
+  // each use is consumed before the next one can start, so no waiter falls
+  // two phases behind.  Items with no query tile (none occur for the shapes
+  // accepted) are skipped by every role alike.
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG0));
     if (warp == 0 && lane == 0 && !abort_all) {
@@ -773,12 +785,8 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         const int st = T % kStages, use = T / kStages;
         if (use > 0 && !mbar_wait(&bar_qempty[st], (use - 1) & 1)) return false;
         mbar_arrive_expect_tx(&bar_qfull[st], 2 * C::kQBytes + 2 * kBM * 4);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(sQ + st * C::kQBytes + c * kQChunk, &tmQ, &bar_qfull[st], c * 64, tile * kBM,
-                      bh);
-          tma_load_3d(sDO + st * C::kQBytes + c * kQChunk, &tmDO, &bar_qfull[st], c * 64,
-                      tile * kBM, bh);
-        }
+        tma_load_3d(sQ + st * C::kQBytes, &tmQ, &bar_qfull[st], 0, tile * kBM, bh);
+        tma_load_3d(sDO + st * C::kQBytes, &tmDO, &bar_qfull[st], 0, tile * kBM, bh);
         const size_t prow = (size_t)bh * Npad + (size_t)tile * kBM;
         bulk_load(sLse + st * kBM, neg_lse2 + prow, kBM * 4, &bar_qfull[st]);
         bulk_load(sDelta + st * kBM, delta + prow, kBM * 4, &bar_qfull[st]);
@@ -790,22 +798,25 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         if (L < 0) break;
         const BwdItem it = item(L);
         if (it.nq == 0) continue;
-        // The item's first Q / dO tile, then K_j and V_j once the previous
-        // item's products (the last to read K and V) have completed.
+        // The item's first Q / dO tile, then K_j and V_j into slot n % 2 once
+        // the item two back, which used that slot, has completed its products.
         if (!load_q(it.i_first, it.bh)) { ok = false; break; }
-        if (items > 0 && !mbar_wait(bar_itemdone, (items - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar_kv, 2 * C::kKVBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(sK + c * kKVChunk, &tmK, bar_kv, c * 64, it.j * kBlockN, it.bh);
-          tma_load_3d(sV + c * kKVChunk, &tmV, bar_kv, c * 64, it.j * kBlockN, it.bh);
+        const int slot = items & 1;
+        if (items >= 2 && !mbar_wait(&bar_kvfree[slot], ((items >> 1) - 1) & 1)) {
+          ok = false;
+          break;
         }
+        mbar_arrive_expect_tx(&bar_kvfull[slot], 2 * C::kKVBytes);
+        tma_load_3d(sK + slot * C::kKVBytes, &tmK, &bar_kvfull[slot], 0, it.j * kBlockN, it.bh);
+        tma_load_3d(sV + slot * C::kKVBytes, &tmV, &bar_kvfull[slot], 0, it.j * kBlockN, it.bh);
         ++items;
         for (int q = 1; q < it.nq; ++q)
           if (!load_q(it.i_first + q, it.bh)) { ok = false; break; }
       }
       if (!ok) set_fail(ATTN_ERR_TIMEOUT);
       // Do not leave while copies into this CTA's shared memory are in flight.
-      if (items > 0) mbar_wait(bar_kv, (items - 1) & 1);
+      for (int x = max(0, items - 2); x < items; ++x)
+        mbar_wait(&bar_kvfull[x & 1], (x >> 1) & 1);
       for (int x = max(0, T - kStages); x < T; ++x)
         mbar_wait(&bar_qfull[x % kStages], (x / kStages) & 1);
     } else if (warp == 1 && !abort_all) {
@@ -814,23 +825,17 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, kBM, false, false);  // K-major A and B
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // TMEM A, MN-major B
       constexpr uint32_t idesc_dq = idesc_bf16(D, kBM, true, true);     // MN-major A and B
-      const uint64_t kK = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t kV = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t kQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t kDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
       const uint64_t mQ = sdesc_sw128(smem_u32(sQ), kQChunk, 1024);
       const uint64_t mDO = sdesc_sw128(smem_u32(sDO), kQChunk, 1024);
-      const uint64_t mK = sdesc_sw128(smem_u32(sK), kKVChunk, 1024);
       const uint64_t mDS = sdesc_sw128(smem_u32(sDS), kDSBytes, 1024);
-      // S^T or dP^T (into column d_col) = X_j Y_i^T over the d head dims.
+      // S^T or dP^T (into column d_col) = X_j Y_i^T over the d = 64 head dims.
       auto issue_xy = [&](uint32_t d_col, uint64_t dX, uint64_t dY, uint32_t y_off) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t cx = (kk >> 2) * kKVChunk + (kk & 3) * 32;
-          const uint32_t cy = (kk >> 2) * kQChunk + (kk & 3) * 32;
-          mma_ss_elect(tmem + d_col, sdesc_add(dX, cx), sdesc_add(dY, y_off + cy), idesc_s,
-                       kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_elect(tmem + d_col, sdesc_add(dX, kk * 32), sdesc_add(dY, y_off + kk * 32),
+                       idesc_s, kk > 0 ? 1u : 0u);
       };
       bool ok = true;
       int T0 = 0, items = 0;
@@ -839,31 +844,35 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         if (L < 0) break;
         const BwdItem it = item(L);
         if (it.nq == 0) continue;
-        // Prologue: S^T(T0), dP^T(T0), S^T(T0+1).  The S buffers, the dP region
-        // and (below) dV / dK are free: the products of the previous item that
-        // read them were issued earlier on this thread, and the compute warps
-        // finished reading dV / dK before producing this item's first P and dS.
-        ok = warp_wait(bar_kv, items & 1);
-        if (ok) ok = warp_wait(&bar_qfull[T0 % kStages], (T0 / kStages) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_xy(C::kColS + (T0 & 1) * kBM, kK, kQ, (T0 % kStages) * C::kQBytes);
-        mma_commit_elect(&bar_sfull[T0 & 1]);
-        issue_xy(C::kColDP, kV, kDO, (T0 % kStages) * C::kQBytes);
-        mma_commit_elect(bar_dpfull);
-        if (it.nq > 1) {
-          const int T1 = T0 + 1;
-          ok = warp_wait(&bar_qfull[T1 % kStages], (T1 / kStages) & 1);
-          if (!ok) break;
+        const int slot = items & 1;
+        const uint64_t kK = sdesc_sw128(smem_u32(sK + slot * C::kKVBytes), 16, 1024);
+        const uint64_t kV = sdesc_sw128(smem_u32(sV + slot * C::kKVBytes), 16, 1024);
+        const uint64_t mK = sdesc_sw128(smem_u32(sK + slot * C::kKVBytes), kKVChunk, 1024);
+        // S^T(T) and dP^T(T) into buffers T % 2, once Q_i / dO_i have landed.
+        auto issue_sdp = [&](int T) -> bool {
+          const int stT = T % kStages;
+          if (!warp_wait(&bar_qfull[stT], (T / kStages) & 1)) return false;
           tc_fence_after();
-          issue_xy(C::kColS + (T1 & 1) * kBM, kK, kQ, (T1 % kStages) * C::kQBytes);
-          mma_commit_elect(&bar_sfull[T1 & 1]);
-        }
+          issue_xy(C::kColS + (T & 1) * kBM, kK, kQ, stT * C::kQBytes);
+          mma_commit_elect(&bar_sfull[T & 1]);
+          issue_xy(C::kColDP + (T & 1) * kBM, kV, kDO, stT * C::kQBytes);
+          mma_commit_elect(&bar_dpfull[T & 1]);
+          return true;
+        };
+        // Prologue: S^T and dP^T of the item's first two tiles.  Their buffers
+        // are free: the products of the previous item that read them (dV and
+        // dK of its last two tiles) were issued earlier on this thread.
+        ok = warp_wait(&bar_kvfull[slot], (items >> 1) & 1);
+        if (!ok) break;
+        if (!issue_sdp(T0)) { ok = false; break; }
+        if (it.nq > 1 && !issue_sdp(T0 + 1)) { ok = false; break; }
         for (int q = 0; q < it.nq && ok; ++q) {
           const int T = T0 + q;
           const int st = T % kStages, b = T & 1;
           const uint32_t so = st * C::kQBytes;
-          // dV += P^T dO_i
+          // dV += P^T dO_i.  The first dV / dK products of an item overwrite the
+          // accumulators: the compute warps signal this item's first P and dS
+          // only after reading the previous item's dV and dK.
           if (!warp_wait(&bar_pready[b], (T >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -875,34 +884,26 @@ __global__ void __launch_bounds__(kThreadsR, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBM / 16; ++kk)
-            mma_ts_elect(tmem + C::kColDK, tmem + C::kColDP + packed_col(kk),
+            mma_ts_elect(tmem + C::kColDK, tmem + C::kColDP + b * kBM + packed_col(kk),
                          sdesc_add(mQ, so + kk * 2048), idesc_acc, (q > 0 || kk > 0) ? 1u : 0u);
           mma_commit_elect(&bar_qempty[st]);
-          // dP^T(T+1): the dP region is free (dK(T) above read dS^T from it).
-          if (q + 1 < it.nq) {
-            issue_xy(C::kColDP, kV, kDO, ((T + 1) % kStages) * C::kQBytes);
-            mma_commit_elect(bar_dpfull);
-          }
-          // dQ^T(T) = K_j^T dS^T(T)
-          if (T > 0 && !warp_wait(bar_dqfree, (T - 1) & 1)) { ok = false; break; }
+          // dQ^T(T) = K_j^T dS^T(T) into dQ buffer b, once the drain warps have
+          // read dQ^T(T-2) from it.
+          if (T >= 2 && !warp_wait(&bar_dqfree[b], ((T >> 1) - 1) & 1)) { ok = false; break; }
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_ss_elect(tmem + C::kColDQ, sdesc_add(mK, kk * 2048),
+            mma_ss_elect(tmem + C::kColDQ + b * kBM, sdesc_add(mK, kk * 2048),
                          sdesc_add(mDS, b * kDSBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
-          mma_commit_elect(bar_dqfull);
+          mma_commit_elect(&bar_dqfull[b]);
           mma_commit_elect(&bar_dqdone[b]);
-          // S^T(T+2) into buffer b (P^T(T) was read by dV(T) above).
-          if (q + 2 < it.nq) {
-            const int T2 = T + 2;
-            if (!warp_wait(&bar_qfull[T2 % kStages], (T2 / kStages) & 1)) { ok = false; break; }
-            tc_fence_after();
-            issue_xy(C::kColS + b * kBM, kK, kQ, (T2 % kStages) * C::kQBytes);
-            mma_commit_elect(&bar_sfull[b]);
-          }
+          // S^T(T+2) and dP^T(T+2) into buffers b: dV(T) and dK(T) above have
+          // read P^T(T) and dS^T(T) from them.
+          if (q + 2 < it.nq && !issue_sdp(T + 2)) { ok = false; break; }
         }
         if (!ok) break;
-        // dV, dK complete; K and V may be replaced.
+        // dV, dK complete; the K / V slot may be refilled.
         mma_commit_elect(bar_itemdone);
+        mma_commit_elect(&bar_kvfree[slot]);
         T0 += it.nq;
         ++items;
       }
@@ -920,16 +921,15 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         if (L < 0) break;
         const BwdItem it = item(L);
         if (it.nq == 0) continue;
-        for (int c = 0; c < C::kChunks && ok; ++c)
-          for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(&bar_epifull[h], es[h] & 1)) { ok = false; break; }
-            tma_store_3d(h == 0 ? &tmDV : &tmDK, smem + C::kOffStage + h * kKVChunk, c * 64,
-                         it.j * kBlockN, it.bh);
-            bulk_commit_group();
-            bulk_wait_group_read0();
-            mbar_arrive(&bar_epifree[h]);
-            ++es[h];
-          }
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(&bar_epifull[h], es[h] & 1)) { ok = false; break; }
+          tma_store_3d(h == 0 ? &tmDV : &tmDK, smem + C::kOffStage + h * kKVChunk, 0,
+                       it.j * kBlockN, it.bh);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&bar_epifree[h]);
+          ++es[h];
+        }
       }
       if (!ok) set_fail(ATTN_ERR_TIMEOUT);
       // The output stores complete before this CTA ends.
@@ -939,13 +939,11 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   } else if (warp >= 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDrain));
     // ------------------------------------------------------------ dQ drain
-    // dQ^T(T), all 64 query columns: each thread adds one head dim of every
-    // query row; a warp's reductions of one column cover contiguous bytes.
-    // d = 128 (M = 128): head dim m is TMEM lane m, 32 per warp.  d = 64
-    // (M = 64): head dim m is lane (m / 16) * 32 + m % 16, so lanes 0-15 of
-    // each warp hold 16 head dims and lanes 16-31 hold nothing of dQ^T.
-    const int dim = D == 128 ? (warp & 3) * 32 + lane : (warp & 3) * 16 + (lane & 15);
-    const bool holds_dim = D == 128 || lane < 16;
+    // dQ^T(T) (M = 64) from dQ buffer T % 2: head dim m is TMEM lane
+    // (m / 16) * 32 + m % 16, so lanes 0-15 of each warp hold 16 head dims
+    // and add them, one query row per reduction (64 contiguous bytes).
+    const int dim = (warp & 3) * 16 + (lane & 15);
+    const bool holds_dim = lane < 16;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tDQ = tmem + lane_off + C::kColDQ;
     bool ok = !abort_all;
@@ -955,17 +953,18 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       if (L < 0) break;
       const BwdItem it = item(L);
       for (int q = 0; q < it.nq && ok; ++q, ++T) {
-        ok = warp_wait(bar_dqfull, T & 1);
+        const int b = T & 1;
+        ok = warp_wait(&bar_dqfull[b], (T >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
         uint32_t acc[2][32];
-        tmem_ld32(tDQ, acc[0]);
-        tmem_ld32(tDQ + 32, acc[1]);
+        tmem_ld32(tDQ + b * kBM, acc[0]);
+        tmem_ld32(tDQ + b * kBM + 32, acc[1]);
         tmem_wait_ld();
         reg_fence(acc[0]);
         reg_fence(acc[1]);
         tc_fence_before();
-        mbar_arrive(bar_dqfree);
+        mbar_arrive(&bar_dqfree[b]);
         float* dst = dqacc + ((size_t)it.bh * Npad + (size_t)(it.i_first + q) * kBM) * D + dim;
         if (holds_dim) {
 #pragma unroll
@@ -987,7 +986,6 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     const int h = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tDP = tmem + lane_off + C::kColDP;
     const uint32_t dsBase0 = smem_u32(sDS);
     const uint32_t aStage = smem_u32(smem + C::kOffStage + h * kKVChunk);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
@@ -1005,6 +1003,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         const int st = T % kStages, b = T & 1;
         const int i = itm.i_first + q;
         const uint32_t tS = tmem + lane_off + C::kColS + b * kBM;
+        const uint32_t tDP = tmem + lane_off + C::kColDP + b * kBM;
         ok = warp_wait(&bar_qfull[st], (T / kStages) & 1);
         if (!ok) break;
         ok = warp_wait(&bar_sfull[b], (T >> 1) & 1);
@@ -1062,7 +1061,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         tc_fence_before();
         mbar_arrive(&bar_pready[b]);
 
-        ok = warp_wait(bar_dpfull, T & 1);
+        ok = warp_wait(&bar_dpfull[b], (T >> 1) & 1);
         if (!ok) break;
         // dS^T buffer b is free once dQ^T(T-2), which read it, has completed.
         if (T >= 2) {
@@ -1108,41 +1107,39 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       }
       if (!ok) break;
       // ------------------------- epilogue: h = 0 writes dV, h = 1 scale * dK
-      // Staged 64 columns at a time in this warpgroup's slot; warp 3 stores
-      // each chunk with TMA.  The next item's first dV / dK products, which
-      // overwrite the accumulators, wait for this warpgroup's next P and dS,
-      // so they cannot run before the accumulators have been read here.
+      // Staged in this warpgroup's slot; warp 3 stores it with TMA.  The next
+      // item's first dV / dK products, which overwrite the accumulators, wait
+      // for this warpgroup's next P and dS, so they cannot run before the
+      // accumulators have been read here.
       ok = warp_wait(bar_itemdone, items & 1);
       if (!ok) break;
       ++items;
       tc_fence_after();
       const uint32_t tAcc = tmem + lane_off + (h == 0 ? C::kColDV : C::kColDK);
       const float mul = h == 0 ? 1.f : scale;
-      for (int c = 0; c < C::kChunks && ok; ++c) {
-        // The slot is free once the previous chunk's store has read it.
-        if (es > 0) {
-          ok = warp_wait(&bar_epifree[h], (es - 1) & 1);
-          if (!ok) break;
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t o[32];
-          tmem_ld32(tAcc + c * 64 + hh * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_shared_v4(aStage + sw128_offset(r, hh * 4 + u), pk[4 * u], pk[4 * u + 1],
-                         pk[4 * u + 2], pk[4 * u + 3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar_epifull[h]);  // warp 3 stores the chunk
-        ++es;
+      // The slot is free once the previous item's store has read it.
+      if (es > 0) {
+        ok = warp_wait(&bar_epifree[h], (es - 1) & 1);
+        if (!ok) break;
       }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t o[32];
+        tmem_ld32(tAcc + hh * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(aStage + sw128_offset(r, hh * 4 + u), pk[4 * u], pk[4 * u + 1],
+                       pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar_epifull[h]);  // warp 3 stores the chunk
+      ++es;
     }
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
   }
