@@ -622,12 +622,23 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 //     the current item runs, and its first products follow the current
 //     item's last ones without a load in between.
 // Per 64-row tile T (b = T % 2) the MMA warp issues dV(T), dK(T), dQ^T(T) into
-// dQ buffer b, then S^T(T+2) and dP^T(T+2) into S and dP buffers b.  dV and dK
-// are staged 64 columns at a time and stored by warp 3 with TMA.
-// kv_full[2], kv_free[2], q_full[3], q_empty[3], s_full[2], p_ready[2],
-// dp_full[2], ds_ready, dq_full[2], dq_free[2], dq_done[2], item_done,
-// mma_final, epi_full[2], epi_free[2]
-constexpr int kNumBarsP = 2 + 2 + 3 + 3 + 2 + 2 + 2 + 1 + 2 + 2 + 2 + 1 + 1 + 2 + 2;
+// dQ buffer b, then S^T(T+2) and dP^T(T+2) into S and dP buffers b.  After an
+// item the drain warps stage dV and scale * dK, and warp 3 stores them with TMA.
+// dV and dK are read out of TMEM by the drain warps, so the compute warps go
+// straight on to the next item's first P.  Measured on the gpt2 workload and
+// not kept: a five-tile Q / dO ring (2.5% slower), issuing dV(T) together with
+// dK(T) (K steps alternating between the two accumulators: 5% slower, as dV
+// then waits for dS), and dQ^T(T) interleaved with S^T(T+2) and dP^T(T+2) (13%
+// slower: the compute warps, not the tensor pipe, set the pace, and S^T(T+2)
+// then completes later).
+// ds_ready is split per buffer like p_ready: with dP^T issued two tiles ahead,
+// the compute warps can finish dS(T+1) before the MMA warp has seen dS(T), so
+// a single barrier could complete twice under a waiter.
+// kv_full[2], kv_free[2], q_full[5], q_empty[5], s_full[2], p_ready[2],
+// dp_full[2], ds_ready[2], dq_full[2], dq_free[2], dq_done[2], item_done,
+// acc_free, mma_final, epi_full[2], epi_free[2]
+constexpr int kStagesP = 3;
+constexpr int kNumBarsP = 2 + 2 + 3 + 3 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 + 2;
 template <int D>
 struct PCfg {
   static_assert(D == 64, "the persistent variant is laid out for d = 64");
@@ -636,12 +647,12 @@ struct PCfg {
   static constexpr int kOffK = 0;                 // two K slots
   static constexpr int kOffV = kOffK + 2 * kKVBytes;  // two V slots
   static constexpr int kOffQ = kOffV + 2 * kKVBytes;
-  static constexpr int kOffDO = kOffQ + kStages * kQBytes;
-  static constexpr int kOffDS = kOffDO + kStages * kQBytes;
+  static constexpr int kOffDO = kOffQ + kStagesP * kQBytes;
+  static constexpr int kOffDS = kOffDO + kStagesP * kQBytes;
   static constexpr int kOffStage = kOffDS + 2 * kDSBytes;
   static constexpr int kOffLse = kOffStage + 2 * kKVChunk;
-  static constexpr int kOffDelta = kOffLse + kStages * kBM * 4;
-  static constexpr int kOffBar = kOffDelta + kStages * kBM * 4;
+  static constexpr int kOffDelta = kOffLse + kStagesP * kBM * 4;
+  static constexpr int kOffBar = kOffDelta + kStagesP * kBM * 4;
   static constexpr int kSmemBytes = kOffBar + kNumBarsP * 8 + 16;
   // TMEM: dV, dK (64 each), S^T, dP^T and dQ^T double-buffered (64 each).
   static constexpr uint32_t kColDV = 0, kColDK = 64, kColS = 128, kColDP = 256, kColDQ = 384;
@@ -701,19 +712,20 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* bar_kvfull = bars + 0;     // [2] K_j / V_j slot loaded
   uint64_t* bar_kvfree = bars + 2;     // [2] every product reading the slot has completed
-  uint64_t* bar_qfull = bars + 4;      // [3]
-  uint64_t* bar_qempty = bars + 7;     // [3]
+  uint64_t* bar_qfull = bars + 4;      // [5]
+  uint64_t* bar_qempty = bars + 7;     // [5]
   uint64_t* bar_sfull = bars + 10;     // [2]
   uint64_t* bar_pready = bars + 12;    // [2]
   uint64_t* bar_dpfull = bars + 14;    // [2]
-  uint64_t* bar_dsready = bars + 16;
-  uint64_t* bar_dqfull = bars + 17;    // [2]
-  uint64_t* bar_dqfree = bars + 19;    // [2]
-  uint64_t* bar_dqdone = bars + 21;    // [2]
-  uint64_t* bar_itemdone = bars + 23;  // every product of an item has completed
-  uint64_t* bar_final = bars + 24;
-  uint64_t* bar_epifull = bars + 25;   // [2] a staged dV / dK chunk is complete
-  uint64_t* bar_epifree = bars + 27;   // [2] its TMA store has read the staging slot
+  uint64_t* bar_dsready = bars + 16;   // [2]
+  uint64_t* bar_dqfull = bars + 18;    // [2]
+  uint64_t* bar_dqfree = bars + 20;    // [2]
+  uint64_t* bar_dqdone = bars + 22;    // [2]
+  uint64_t* bar_itemdone = bars + 24;  // every product of an item has completed
+  uint64_t* bar_accfree = bars + 25;   // the drain warps have read dV and dK out of TMEM
+  uint64_t* bar_final = bars + 26;
+  uint64_t* bar_epifull = bars + 27;   // [2] a staged dV / dK chunk is complete
+  uint64_t* bar_epifree = bars + 29;   // [2] its TMA store has read the staging slot
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarsP);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -721,7 +733,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
     *s_abort = (smem_u32(smem) & 1023u) != 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStagesP; ++s) {
       mbar_init(&bar_qfull[s], 1);
       mbar_init(&bar_qempty[s], 1 + 8);  // MMA commit + one arrive per compute warp
     }
@@ -731,14 +743,15 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       mbar_init(&bar_sfull[b], 1);
       mbar_init(&bar_pready[b], 256);
       mbar_init(&bar_dpfull[b], 1);
+      mbar_init(&bar_dsready[b], 256);
       mbar_init(&bar_dqfull[b], 1);
       mbar_init(&bar_dqfree[b], 128);
       mbar_init(&bar_dqdone[b], 1);
       mbar_init(&bar_epifull[b], 128);
       mbar_init(&bar_epifree[b], 1);
     }
-    mbar_init(bar_dsready, 256);
     mbar_init(bar_itemdone, 1);
+    mbar_init(bar_accfree, 128);
     mbar_init(bar_final, 1);
     fence_mbar_init();
   }
@@ -782,7 +795,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       bool ok = true;
       int T = 0, items = 0;
       auto load_q = [&](int tile, int bh) -> bool {
-        const int st = T % kStages, use = T / kStages;
+        const int st = T % kStagesP, use = T / kStagesP;
         if (use > 0 && !mbar_wait(&bar_qempty[st], (use - 1) & 1)) return false;
         mbar_arrive_expect_tx(&bar_qfull[st], 2 * C::kQBytes + 2 * kBM * 4);
         tma_load_3d(sQ + st * C::kQBytes, &tmQ, &bar_qfull[st], 0, tile * kBM, bh);
@@ -817,8 +830,8 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       // Do not leave while copies into this CTA's shared memory are in flight.
       for (int x = max(0, items - 2); x < items; ++x)
         mbar_wait(&bar_kvfull[x & 1], (x >> 1) & 1);
-      for (int x = max(0, T - kStages); x < T; ++x)
-        mbar_wait(&bar_qfull[x % kStages], (x / kStages) & 1);
+      for (int x = max(0, T - kStagesP); x < T; ++x)
+        mbar_wait(&bar_qfull[x % kStagesP], (x / kStagesP) & 1);
     } else if (warp == 1 && !abort_all) {
       // ------------------------------------------------------------ MMA issuer
       // Whole warp, warp-uniform operands; elect.sync picks the issuing lane.
@@ -850,8 +863,8 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         const uint64_t mK = sdesc_sw128(smem_u32(sK + slot * C::kKVBytes), kKVChunk, 1024);
         // S^T(T) and dP^T(T) into buffers T % 2, once Q_i / dO_i have landed.
         auto issue_sdp = [&](int T) -> bool {
-          const int stT = T % kStages;
-          if (!warp_wait(&bar_qfull[stT], (T / kStages) & 1)) return false;
+          const int stT = T % kStagesP;
+          if (!warp_wait(&bar_qfull[stT], (T / kStagesP) & 1)) return false;
           tc_fence_after();
           issue_xy(C::kColS + (T & 1) * kBM, kK, kQ, stT * C::kQBytes);
           mma_commit_elect(&bar_sfull[T & 1]);
@@ -868,19 +881,23 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         if (it.nq > 1 && !issue_sdp(T0 + 1)) { ok = false; break; }
         for (int q = 0; q < it.nq && ok; ++q) {
           const int T = T0 + q;
-          const int st = T % kStages, b = T & 1;
+          const int st = T % kStagesP, b = T & 1;
           const uint32_t so = st * C::kQBytes;
           // dV += P^T dO_i.  The first dV / dK products of an item overwrite the
-          // accumulators: the compute warps signal this item's first P and dS
-          // only after reading the previous item's dV and dK.
+          // accumulators, so they wait until the drain warps have read the
+          // previous item's dV and dK out of TMEM.
           if (!warp_wait(&bar_pready[b], (T >> 1) & 1)) { ok = false; break; }
+          if (q == 0 && items > 0 && !warp_wait(bar_accfree, (items - 1) & 1)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBM / 16; ++kk)
             mma_ts_elect(tmem + C::kColDV, tmem + C::kColS + b * kBM + packed_col(kk),
                          sdesc_add(mDO, so + kk * 2048), idesc_acc, (q > 0 || kk > 0) ? 1u : 0u);
           // dK += dS^T Q_i
-          if (!warp_wait(bar_dsready, T & 1)) { ok = false; break; }
+          if (!warp_wait(&bar_dsready[b], (T >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBM / 16; ++kk)
@@ -946,12 +963,14 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     const bool holds_dim = lane < 16;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tDQ = tmem + lane_off + C::kColDQ;
+    const int r = (warp & 3) * 32 + lane;  // key row = TMEM lane, for the dV / dK epilogue
     bool ok = !abort_all;
-    int T = 0;
+    int T = 0, items = 0, es = 0;
     for (int rr = 0; ok; ++rr) {
       const int L = item_of(rr, total);
       if (L < 0) break;
       const BwdItem it = item(L);
+      if (it.nq == 0) continue;
       for (int q = 0; q < it.nq && ok; ++q, ++T) {
         const int b = T & 1;
         ok = warp_wait(&bar_dqfull[b], (T >> 1) & 1);
@@ -974,6 +993,46 @@ __global__ void __launch_bounds__(kThreadsR, 1)
                          : "memory");
         }
       }
+      if (!ok) break;
+      // ------------------------ epilogue: dV and scale * dK of the item
+      // Once every product of the item has completed, read dV and dK out of
+      // TMEM (32 columns at a time), release the accumulators to the next
+      // item's products, and stage them as BF16 for warp 3's TMA stores.
+      ok = warp_wait(bar_itemdone, items & 1);
+      if (!ok) break;
+      ++items;
+      tc_fence_after();
+      if (es > 0) {
+        ok = warp_wait(&bar_epifree[0], (es - 1) & 1) && warp_wait(&bar_epifree[1], (es - 1) & 1);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t tAcc = tmem + lane_off + (h == 0 ? C::kColDV : C::kColDK);
+        const uint32_t aStage = smem_u32(smem + C::kOffStage + h * kKVChunk);
+        const float mul = h == 0 ? 1.f : scale;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t o[32];
+          tmem_ld32(tAcc + hh * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(aStage + sw128_offset(r, hh * 4 + u), pk[4 * u], pk[4 * u + 1],
+                         pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_accfree);  // the next item's dV / dK products may overwrite them
+      fence_proxy_async_smem();
+      mbar_arrive(&bar_epifull[0]);  // warp 3 stores dV
+      mbar_arrive(&bar_epifull[1]);  // and dK
+      ++es;
     }
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
   } else {
@@ -981,16 +1040,14 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     // ------------------------------------------- P and dS (two warpgroups)
     // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) owns query columns
     // [32h, 32h+32) of every 64-row tile: it computes those columns of P^T
-    // and dS^T (thread = key row = TMEM lane).  After an item it writes dV
-    // (h = 0) or scale * dK (h = 1).
+    // and dS^T (thread = key row = TMEM lane).
     const int h = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t dsBase0 = smem_u32(sDS);
-    const uint32_t aStage = smem_u32(smem + C::kOffStage + h * kKVChunk);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = !abort_all;
-    int T = 0, items = 0, es = 0;
+    int T = 0;
     for (int rr = 0; ok; ++rr) {
       const int L = item_of(rr, total);
       if (L < 0) break;
@@ -1000,11 +1057,11 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       const int kv = j * kBlockN + r;
       const bool key_valid = kv < N;
       for (int q = 0; q < itm.nq && ok; ++q, ++T) {
-        const int st = T % kStages, b = T & 1;
+        const int st = T % kStagesP, b = T & 1;
         const int i = itm.i_first + q;
         const uint32_t tS = tmem + lane_off + C::kColS + b * kBM;
         const uint32_t tDP = tmem + lane_off + C::kColDP + b * kBM;
-        ok = warp_wait(&bar_qfull[st], (T / kStages) & 1);
+        ok = warp_wait(&bar_qfull[st], (T / kStagesP) & 1);
         if (!ok) break;
         ok = warp_wait(&bar_sfull[b], (T >> 1) & 1);
         if (!ok) break;
@@ -1101,45 +1158,10 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar_dsready);
+        mbar_arrive(&bar_dsready[b]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_qempty[st]);
       }
-      if (!ok) break;
-      // ------------------------- epilogue: h = 0 writes dV, h = 1 scale * dK
-      // Staged in this warpgroup's slot; warp 3 stores it with TMA.  The next
-      // item's first dV / dK products, which overwrite the accumulators, wait
-      // for this warpgroup's next P and dS, so they cannot run before the
-      // accumulators have been read here.
-      ok = warp_wait(bar_itemdone, items & 1);
-      if (!ok) break;
-      ++items;
-      tc_fence_after();
-      const uint32_t tAcc = tmem + lane_off + (h == 0 ? C::kColDV : C::kColDK);
-      const float mul = h == 0 ? 1.f : scale;
-      // The slot is free once the previous item's store has read it.
-      if (es > 0) {
-        ok = warp_wait(&bar_epifree[h], (es - 1) & 1);
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t o[32];
-        tmem_ld32(tAcc + hh * 32, o);
-        tmem_wait_ld();
-        reg_fence(o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(aStage + sw128_offset(r, hh * 4 + u), pk[4 * u], pk[4 * u + 1],
-                       pk[4 * u + 2], pk[4 * u + 3]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bar_epifull[h]);  // warp 3 stores the chunk
-      ++es;
     }
     if (!ok) set_fail(ATTN_ERR_TIMEOUT);
   }
