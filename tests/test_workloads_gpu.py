@@ -34,9 +34,13 @@ def _dev(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def _check(A, w, x, heads, delta_bound=False):
+def _check(A, w, x, heads, delta_bound=False, beta=None):
     t = {k: _dev(v) for k, v in x.items()}
-    o, lse = A.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
+    if beta is None:
+        o, lse = A.attn_fwd(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal)
+    else:
+        o, lse = A.attn_fwd_stable(t["q"], t["k"], t["v"], scale=w.scale, causal=w.causal,
+                                   beta=beta)
     dq, dk, dv = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=w.scale,
                             causal=w.causal)
     A.attn_check_status()
@@ -97,3 +101,14 @@ def test_lowrank_shape(A, sigma):
 def test_longseq_shape(A):
     w = inputs.WORKLOADS["longseq"]
     _check(A, w, inputs.make_inputs(w, seed=0), heads=[w.B * w.H - 1])
+
+
+@pytest.mark.parametrize("beta", [None, 2.0], ids=["plain", "stable"])
+@pytest.mark.parametrize("sigma", [1.0, 4.0, 16.0])
+def test_lowrank_ties_shape(A, sigma, beta):
+    """The exact-tie stress workload at full size (B4 H16 N2048 d128, key rows
+    duplicated in pairs so that row maxima repeat exactly), plain and with the
+    stabilised normaliser; the backward runs from each forward's LSE."""
+    w = inputs.WORKLOADS["lowrank_ties"]
+    _check(A, w, inputs.make_inputs(w, seed=0, sigma=sigma), heads=[0, w.B * w.H - 1],
+           delta_bound=sigma > 1.0, beta=beta)
