@@ -37,6 +37,15 @@ namespace attn {
 
 static __device__ unsigned int g_status_bwd;
 
+#ifdef ATTN_TEST_HOOKS
+// Test instrumentation, compiled only into the separate test build of the
+// library (ATTN_TEST_HOOKS), never into libattn.so: when g_hook_stall_bwd is
+// set, the first P/dS warpgroup of CTA 0 of the backward main kernel first
+// waits on a barrier that nothing ever arrives at, so the wait runs out
+// (after the test build's short limit) and the kernel takes its failure path.
+static __device__ int g_hook_stall_bwd;
+#endif
+
 namespace {
 
 __device__ __forceinline__ void set_fail(unsigned int code) { atomicOr(&g_status_bwd, code); }
@@ -246,6 +255,9 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     mbar_init(bar_dqfree, 128);
     mbar_init(bar_dkvdone, 1);
     mbar_init(bar_final, 1);
+#ifdef ATTN_TEST_HOOKS
+    mbar_init(reinterpret_cast<uint64_t*>(tmem_slot + 2), 1);  // nothing arrives here
+#endif
     mbar_init(bar_epi_dv, 128);
     mbar_init(bar_epi_dk, 128);
     fence_mbar_init();
@@ -446,6 +458,10 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     const uint32_t dsBase0 = smem_u32(sDS);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = !abort_all;
+#ifdef ATTN_TEST_HOOKS
+    if (ok && g_hook_stall_bwd && blockIdx.x == 0 && h == 0)
+      ok = warp_wait(reinterpret_cast<uint64_t*>(tmem_slot + 2), 0);
+#endif
     for (int it = 0; it < nq && ok; ++it) {
       const int st = it % kStages, b = it & 1;
       const int i = i_first + it;
@@ -753,6 +769,9 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     mbar_init(bar_itemdone, 1);
     mbar_init(bar_accfree, 128);
     mbar_init(bar_final, 1);
+#ifdef ATTN_TEST_HOOKS
+    mbar_init(reinterpret_cast<uint64_t*>(tmem_slot + 2), 1);  // nothing arrives here
+#endif
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -1047,6 +1066,10 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     const uint32_t dsBase0 = smem_u32(sDS);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = !abort_all;
+#ifdef ATTN_TEST_HOOKS
+    if (ok && g_hook_stall_bwd && blockIdx.x == 0 && h == 0)
+      ok = warp_wait(reinterpret_cast<uint64_t*>(tmem_slot + 2), 0);
+#endif
     int T = 0;
     for (int rr = 0; ok; ++rr) {
       const int L = item_of(rr, total);
@@ -1294,6 +1317,12 @@ cudaError_t launch_bwd_main_bf16(const Problem& p, const void* q, const void* k,
   return p.causal ? main_persistent_impl<64, true>(p, maps, ws, stream)
                   : main_persistent_impl<64, false>(p, maps, ws, stream);
 }
+
+#ifdef ATTN_TEST_HOOKS
+extern "C" ATTN_API int attn_testhook_stall_bwd(int on) {
+  return (int)cudaMemcpyToSymbol(g_hook_stall_bwd, &on, sizeof(on));
+}
+#endif
 
 cudaError_t read_and_clear_status_bwd(unsigned int* out, cudaStream_t stream) {
   static const unsigned int zero = 0;

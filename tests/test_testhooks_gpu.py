@@ -14,10 +14,12 @@ every in-kernel wait.  libattn.so never contains any of it.
    forward on inputs where every row's maximum is attained at least twice,
    including maxima of 0, of tiny size and of either sign; at least two per
    row for the plain forward.
-2. The real forward kernel's failure path: a wait that runs out must make
-   the kernel wind down (copies and MMAs in flight completed, TMEM freed),
+2. The real kernels' failure path: a wait that runs out must make the
+   kernel wind down (copies and MMAs in flight completed, TMEM freed),
    attn_check_status must report ATTN_ERR_TIMEOUT, and the next call must
-   again match the oracle.
+   again match the oracle.  Covered for the forward kernel and for both
+   backward main kernels (the d = 128 one and the persistent d = 64 one),
+   each with one P/dS warpgroup of CTA 0 held on a barrier nothing arrives at.
 """
 import ctypes
 import math
@@ -41,9 +43,12 @@ def T(cuda_device):
     lib.attn_testhook_pbar_counter.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong]
     lib.attn_testhook_stall.restype = ctypes.c_int
     lib.attn_testhook_stall.argtypes = [ctypes.c_int]
+    lib.attn_testhook_stall_bwd.restype = ctypes.c_int
+    lib.attn_testhook_stall_bwd.argtypes = [ctypes.c_int]
     yield lib
     lib.attn_testhook_pbar_counter(None, 0)
     lib.attn_testhook_stall(0)
+    lib.attn_testhook_stall_bwd(0)
 
 
 def _dev(bits):
@@ -159,3 +164,52 @@ def test_forced_wait_timeout_winds_down_and_the_next_call_is_exact(T):
         dev = deviation(og[h], o_ref)
         assert dev["max_abs"] <= 2e-2 and dev["mean_abs"] <= 2e-3, (h, dev)
         assert np.abs(lg[h] - lse_ref).max() <= 1e-3, h
+
+
+def _bwd(T, t, o, lse, scale, causal):
+    B, H, N, d = t["q"].shape
+    out = [torch.full_like(o, float("nan")) for _ in range(3)]
+    ws = torch.empty(int(T.attn_bwd_workspace_bytes(B, H, N, d, 0)), dtype=torch.uint8,
+                     device=o.device)
+    r = T.attn_bwd(t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(), o.data_ptr(),
+                   lse.data_ptr(), t["do"].data_ptr(), out[0].data_ptr(), out[1].data_ptr(),
+                   out[2].data_ptr(), B, H, N, d, ctypes.c_float(scale), int(causal), 0,
+                   ws.data_ptr(), ws.numel(), _stream())
+    assert r == 0, T.attn_last_error()
+    return out
+
+
+def _rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)], ids=["d128_causal", "d64_full"])
+def test_forced_backward_wait_timeout_winds_down_and_the_next_call_is_exact(T, d, causal):
+    # d = 128 runs the one-item-per-CTA backward main kernel, d = 64 the
+    # persistent one; both take the same failure path from the held warpgroup.
+    from precision_numerics_gb300 import attn
+    B, H, N = 1, 4, 1024
+    scale = d ** -0.5
+    x = inputs.random_qkv(33 + d, B, H, N, d)
+    t = {n: _dev(v) for n, v in x.items()}
+    o, lse = attn.attn_fwd(t["q"], t["k"], t["v"], scale=scale, causal=causal)
+    assert T.attn_check_status(_stream()) == 0
+    assert T.attn_testhook_stall_bwd(1) == 0
+    try:
+        _bwd(T, t, o, lse, scale, causal)
+        # the kernel returned (no hang, no fault) and recorded the timeout
+        assert T.attn_check_status(_stream()) == 4, T.attn_last_error()
+    finally:
+        assert T.attn_testhook_stall_bwd(0) == 0
+    assert T.attn_check_status(_stream()) == 0  # the status word was cleared
+    got = _bwd(T, t, o, lse, scale, causal)
+    assert T.attn_check_status(_stream()) == 0, T.attn_last_error()
+    og = o.float().cpu().numpy().reshape(B * H, N, d)
+    g = [x_.float().cpu().numpy().reshape(B * H, N, d) for x_ in got]
+    f = {n: inputs.bf16_bits_to_f32(v).reshape(B * H, N, d) for n, v in x.items()}
+    for h in (0, B * H - 1):  # CTA 0's head and the last one
+        ref = oracle.backward(f["q"][h], f["k"][h], f["v"][h], f["do"][h], scale, causal,
+                              o_for_delta=og[h])
+        for name, gv, rv in zip(("dq", "dk", "dv"), g, ref):
+            assert np.isfinite(gv[h]).all(), (h, name)
+            assert _rel_l2(gv[h], rv) <= 1e-2, (h, name, _rel_l2(gv[h], rv))
