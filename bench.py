@@ -45,7 +45,8 @@ METRIC = "BF16 attention fwd/bwd TFLOP/s on 1 GB300, % of tensor peak; max err v
 UNIT = "TFLOP/s"
 DOMINANT = "bwd_main_kernel"
 DOMINANT_SRC = os.path.join(ROOT, "precision_numerics_gb300", "csrc", "bwd_bf16.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "bwd_main_kernel_llama7b.md")
+# ncu summary of the dominant kernel per workload (DRAM traffic per launch).
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "bwd_main_kernel_{workload}.md")
 
 
 def _peaks():
@@ -153,12 +154,12 @@ def _source_sha():
 
 def _traffic_per_launch(workload: str):
     try:
-        text = open(TRAFFIC_FILE).read()
+        text = open(TRAFFIC_FILE.format(workload=workload)).read()
     except OSError:
         return None
-    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    m_s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_w = re.search(r"workload:\s*(\w+)", text)
+    m_b = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*$", text, re.M)
+    m_s = re.search(r"^source_sha256:\s*([0-9a-f]{64})\s*$", text, re.M)
+    m_w = re.search(r"^workload:\s*(\w+)\s*$", text, re.M)
     if not (m_b and m_s and m_w) or m_s.group(1) != _source_sha() or m_w.group(1) != workload:
         return None
     return float(m_b.group(1))

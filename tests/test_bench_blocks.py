@@ -56,3 +56,17 @@ def test_deviation_block_compares_with_oracle_and_naive():
     # delta stored in FP32: within FP32 rounding of the exact value
     assert blk["delta_lp_minus_delta"]["max_abs"] <= 1e-6 * np.abs(d_exact).max() + 1e-12
     assert set(blk) >= {"tiled_gpu", "naive_bf16", "delta_lp_minus_delta", "sample"}
+
+
+def test_traffic_comes_from_the_workloads_own_profile_and_only_for_the_current_source():
+    import bench
+    for w in ("llama7b", "gpt2"):
+        t = bench._traffic_per_launch(w)
+        assert t is not None and t > 0, w
+    assert bench._traffic_per_launch("longseq") is None  # no committed capture
+    real = bench._source_sha
+    try:
+        bench._source_sha = lambda: "0" * 64  # the kernel source changed since the capture
+        assert bench._traffic_per_launch("llama7b") is None
+    finally:
+        bench._source_sha = real
