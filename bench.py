@@ -436,6 +436,9 @@ def run_ours(args, w):
             "clocks": sampler.summary(),
         }
         line["fwd_tflops"] = _fwd_only_tflops(attn, t, o, lse, w, stream, torch)
+        graph_ms = _graph_step_ms(step, torch, reps=min(args.steps, 200))
+        line["step_graph"] = {"ms_per_step": graph_ms, "eager_ms_per_step": ms_per_step,
+                              "eager_over_graph": ms_per_step / graph_ms}
         line["deviation"] = _deviation_block(w, f, o, dv, ws, o_ref, g_ref[2])
         line["host_us_per_call"] = _host_cost(attn, w, dev, torch)
         if world == 1 and not args.no_cpu_baseline:
@@ -445,6 +448,32 @@ def run_ours(args, w):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def _graph_step_ms(step, torch, reps):
+    """The same device-resident step captured once as a CUDA graph and
+    replayed (milliseconds per step, CUDA events), after the timed region:
+    next to the eagerly issued step it shows what the per-call host work of
+    the four launches costs the step, if anything."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
 
 
 def _host_cost(attn, w, dev, torch, calls=200):
