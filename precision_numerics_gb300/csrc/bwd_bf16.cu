@@ -152,6 +152,9 @@ constexpr int kBM = 64;                    // query rows per tile
 constexpr int kThreadsR = 512;             // + warps 12-15: dQ drain
 constexpr int kRegsWG0 = 96, kRegsCompute = 168, kRegsDrain = 80;  // setmaxnreg split
 static_assert(kRegsWG0 + 2 * kRegsCompute + kRegsDrain <= 512, "split exceeds the launch pool");
+// A 512-thread launch gives 128 registers per thread: setmaxnreg.dec must ask
+// for fewer, setmaxnreg.inc for more.
+static_assert(kRegsWG0 <= 128 && kRegsDrain <= 128 && kRegsCompute >= 128, "setmaxnreg directions");
 constexpr int kStages = 3;                 // Q / dO ring depth
 constexpr int kKVChunk = 128 * 128;        // one 64-column chunk of K_j / V_j (128 rows)
 constexpr int kQChunk = kBM * 128;         // one 64-column chunk of Q_i / dO_i (64 rows)

@@ -58,6 +58,9 @@ constexpr int kThreads = 512;
 // register split (setmaxnreg) that goes with it.
 constexpr int kCorrChunks = 1;
 constexpr int kRegsWG0 = 80, kRegsCorr = 80, kRegsSoftmax = 176;  // 80 + 80 + 2 * 176 <= 512
+// A 512-thread launch gives 128 registers per thread: setmaxnreg.dec must ask
+// for fewer, setmaxnreg.inc for more.
+static_assert(kRegsWG0 <= 128 && kRegsCorr <= 128 && kRegsSoftmax >= 128, "setmaxnreg directions");
 
 template <int D>
 struct FwdCfg {
