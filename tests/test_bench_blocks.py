@@ -58,15 +58,19 @@ def test_deviation_block_compares_with_oracle_and_naive():
     assert set(blk) >= {"tiled_gpu", "naive_bf16", "delta_lp_minus_delta", "sample"}
 
 
-def test_traffic_comes_from_the_workloads_own_profile_and_only_for_the_current_source():
+def test_traffic_comes_from_the_workloads_own_profile_and_only_for_the_current_source(tmp_path):
     import bench
-    for w in ("llama7b", "gpt2"):
-        t = bench._traffic_per_launch(w)
-        assert t is not None and t > 0, w
-    assert bench._traffic_per_launch("longseq") is None  # no committed capture
-    real = bench._source_sha
+    sha = bench._source_sha()
+    (tmp_path / "bwd_main_kernel_gpt2.md").write_text(
+        "History on this workload: 128-row query tiles\n\n"
+        f"traffic_bytes_per_launch: 82265600\nworkload: gpt2\nsource_sha256: {sha}\n")
+    (tmp_path / "bwd_main_kernel_llama7b.md").write_text(
+        f"traffic_bytes_per_launch: 1000\nworkload: llama7b\nsource_sha256: {'0' * 64}\n")
+    real = bench.TRAFFIC_FILE
     try:
-        bench._source_sha = lambda: "0" * 64  # the kernel source changed since the capture
-        assert bench._traffic_per_launch("llama7b") is None
+        bench.TRAFFIC_FILE = str(tmp_path / "bwd_main_kernel_{workload}.md")
+        assert bench._traffic_per_launch("gpt2") == 82265600.0  # this workload's own file
+        assert bench._traffic_per_launch("llama7b") is None     # taken from another source
+        assert bench._traffic_per_launch("longseq") is None     # no capture at all
     finally:
-        bench._source_sha = real
+        bench.TRAFFIC_FILE = real
