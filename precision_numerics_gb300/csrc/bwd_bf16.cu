@@ -1264,10 +1264,11 @@ cudaError_t main_r64_impl(const Problem& p, const CUtensorMap* maps, const BwdWo
 
 // d = 64: persistent CTAs, one per SM, walking the (head, key tile) items in
 // snake order.  The list is ordered heaviest first across all heads (one
-// group): a static schedule over head groups left late heavy items.  On the
-// gpt2 workload this kernel runs the backward main phase in 66 us against 74
-// for one CTA per item; at d = 128 persistence measured slower (311 against
-// 295 us on the llama7b workload), so d = 128 keeps one CTA per item.
+// group): a static schedule over head groups left late heavy items.  When it
+// was introduced it ran the gpt2 workload's backward main phase in 66 us
+// against 74 for one CTA per item (61 us with the double-buffered products
+// it has now); at d = 128 persistence measured slower (311 against 295 us on
+// the llama7b workload), so d = 128 keeps one CTA per item.
 template <int D, bool CAUSAL>
 cudaError_t main_persistent_impl(const Problem& p, const CUtensorMap* maps, const BwdWorkspace& ws,
                                  cudaStream_t stream) {
