@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(256)
 //   dV      += P^T dO_i      M=128 N=d  K=64    TS  (P^T in the S buffer)
 //   dK      += dS^T Q_i      M=128 N=d  K=64    TS  (dS^T in the dP region)
 //   dQ^T(it) = K_j^T dS^T    M=d   N=64 K=128   SS  (dS^T from shared memory)
-// issued in the order dV(it), dK(it), dP^T(it+1), dQ^T(it), S^T(it+2), so the
+// issued in the order dV(it), dK(it), dP^T(it+1), S^T(it+2), dQ^T(it), so the
 // P and dS work of tile it+1 runs while the tensor pipe finishes tile it.
 // dQ^T puts head-dim index d on the TMEM lanes: each drain thread owns one d,
 // and a warp's reductions into the FP32 accumulator cover contiguous bytes of
@@ -388,6 +388,15 @@ __global__ void __launch_bounds__(kThreadsR, 1)
           issue_xy(C::kColDP, kV, kDO, ((it + 1) % kStages) * C::kQBytes);
           mma_commit_elect(bar_dpfull);
         }
+        // S^T(it+2) into buffer b (P^T(it) was read by dV(it) above), ahead of
+        // dQ^T(it), which no compute warp waits for.
+        if (it + 2 < nq) {
+          const int st2 = (it + 2) % kStages;
+          if (!warp_wait(&bar_qfull[st2], ((it + 2) / kStages) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_xy(C::kColS + b * kBM, kK, kQ, st2 * C::kQBytes);
+          mma_commit_elect(&bar_sfull[b]);
+        }
         // dQ^T(it) = K_j^T dS^T(it)
         if (it > 0 && !warp_wait(bar_dqfree, (it - 1) & 1)) { ok = false; break; }
 #pragma unroll
@@ -396,14 +405,6 @@ __global__ void __launch_bounds__(kThreadsR, 1)
                        sdesc_add(mDS, b * kDSBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
         mma_commit_elect(bar_dqfull);
         mma_commit_elect(&bar_dqdone[b]);
-        // S^T(it+2) into buffer b (P^T(it) was read by dV(it) above).
-        if (it + 2 < nq) {
-          const int st2 = (it + 2) % kStages;
-          if (!warp_wait(&bar_qfull[st2], ((it + 2) / kStages) & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_xy(C::kColS + b * kBM, kK, kQ, st2 * C::kQBytes);
-          mma_commit_elect(&bar_sfull[b]);
-        }
       }
       if (ok) mma_commit_elect(bar_dkvdone);
       else if (lane == 0) set_fail(ATTN_ERR_TIMEOUT);
@@ -640,8 +641,8 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 //   - K_j and V_j are double-buffered, so the next item's K and V load while
 //     the current item runs, and its first products follow the current
 //     item's last ones without a load in between.
-// Per 64-row tile T (b = T % 2) the MMA warp issues dV(T), dK(T), dQ^T(T) into
-// dQ buffer b, then S^T(T+2) and dP^T(T+2) into S and dP buffers b.  After an
+// Per 64-row tile T (b = T % 2) the MMA warp issues dV(T), dK(T), S^T(T+2) and
+// dP^T(T+2) into S and dP buffers b, then dQ^T(T) into dQ buffer b.  After an
 // item the drain warps stage dV and scale * dK, and warp 3 stores them with TMA.
 // dV and dK are read out of TMEM by the drain warps, so the compute warps go
 // straight on to the next item's first P.  Measured on the gpt2 workload and
@@ -926,6 +927,10 @@ __global__ void __launch_bounds__(kThreadsR, 1)
             mma_ts_elect(tmem + C::kColDK, tmem + C::kColDP + b * kBM + packed_col(kk),
                          sdesc_add(mQ, so + kk * 2048), idesc_acc, (q > 0 || kk > 0) ? 1u : 0u);
           mma_commit_elect(&bar_qempty[st]);
+          // S^T(T+2) and dP^T(T+2) into buffers b: dV(T) and dK(T) above have
+          // read P^T(T) and dS^T(T) from them.  Issued ahead of dQ^T(T), which
+          // no compute warp waits for (61.4 -> 61.1 us on the gpt2 workload).
+          if (q + 2 < it.nq && !issue_sdp(T + 2)) { ok = false; break; }
           // dQ^T(T) = K_j^T dS^T(T) into dQ buffer b, once the drain warps have
           // read dQ^T(T-2) from it.
           if (T >= 2 && !warp_wait(&bar_dqfree[b], ((T >> 1) - 1) & 1)) { ok = false; break; }
@@ -935,9 +940,6 @@ __global__ void __launch_bounds__(kThreadsR, 1)
                          sdesc_add(mDS, b * kDSBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
           mma_commit_elect(&bar_dqfull[b]);
           mma_commit_elect(&bar_dqdone[b]);
-          // S^T(T+2) and dP^T(T+2) into buffers b: dV(T) and dK(T) above have
-          // read P^T(T) and dS^T(T) from them.
-          if (q + 2 < it.nq && !issue_sdp(T + 2)) { ok = false; break; }
         }
         if (!ok) break;
         // dV, dK complete; the K / V slot may be refilled.

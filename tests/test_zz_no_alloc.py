@@ -95,3 +95,27 @@ def test_python_binding_at_the_largest_listed_problem(lib):
         assert bool(torch.isfinite(g.float()).all()), name
         assert _rel_l2(g, r) <= 1e-2, (name, _rel_l2(g, r))
     assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+
+
+def test_matches_the_oracle(lib):
+    """The no-allocation backward against the FP64 definition directly (not only
+    against attn_bwd): B1 H2 N700 d128 causal and d64 full, every head, dQ, dK,
+    dV within the stated relative L2 of 1e-2."""
+    import oracle
+    from precision_numerics_gb300 import attn, inputs
+    from precision_numerics_gb300.deviation import deviation
+    for seed, (B, H, N, d), causal in ((21, (1, 2, 700, 128), True), (22, (1, 2, 700, 64), False)):
+        x = inputs.random_qkv(seed, B, H, N, d)
+        t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in x.items()}
+        scale = d ** -0.5
+        o, lse = attn.attn_fwd(t["q"], t["k"], t["v"], scale=scale, causal=causal)
+        got = [torch.full_like(o, float("nan")) for _ in range(3)]
+        attn.attn_bwd_noalloc(t["q"], t["k"], t["v"], o, lse, t["do"], *got, scale=scale,
+                              causal=causal)
+        attn.attn_check_status()
+        f = {k: inputs.bf16_bits_to_f32(v).reshape(B * H, N, d) for k, v in x.items()}
+        for h in range(B * H):
+            ref = oracle.backward(f["q"][h], f["k"][h], f["v"][h], f["do"][h], scale, causal)
+            for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+                e = deviation(g.reshape(B * H, N, d)[h].float().cpu().numpy().astype(np.float64), r)
+                assert e["rel_l2"] <= 1e-2, (d, h, name, e)
