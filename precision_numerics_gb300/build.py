@@ -9,6 +9,8 @@ header is newer than the library.
 """
 from __future__ import annotations
 
+import contextlib
+import fcntl
 import glob
 import os
 import shutil
@@ -64,11 +66,33 @@ def needs_build(variant: str = "") -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
+@contextlib.contextmanager
+def _build_lock():
+    """Exclusive lock on _lib/.build.lock: processes that build at the same time
+    (one per rank under torchrun, say) take turns, so none links objects that
+    another one is still writing."""
+    os.makedirs(LIB_DIR, exist_ok=True)
+    with open(os.path.join(LIB_DIR, ".build.lock"), "w") as fh:
+        fcntl.flock(fh, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(fh, fcntl.LOCK_UN)
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
     """Compile and link libattn.so (or libattn_<variant>.so); returns its path."""
     lib = lib_path(variant)
     if not force and not needs_build(variant):
         return lib
+    with _build_lock():
+        # Another process may have built it while this one waited for the lock.
+        if not force and not needs_build(variant):
+            return lib
+        return _build_locked(lib, verbose, extra_flags, variant)
+
+
+def _build_locked(lib, verbose, extra_flags, variant) -> str:
     nvcc = _nvcc()
     build_dir = BUILD if not variant else BUILD + "_" + variant
     os.makedirs(build_dir, exist_ok=True)
@@ -87,7 +111,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: s
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = lib + ".tmp"
+    tmp = f"{lib}.tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
